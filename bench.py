@@ -1,0 +1,316 @@
+"""Benchmark of the W4A16 routed-MoE block on GB300: single-token decode at production width
+(hidden 2048, 256 experts top-8, expert/shared intermediate 512, int4 experts, int8 router/shared, g64).
+
+A step is one forward call: one token through one whole block (router -> top-8 -> experts -> shared ->
+combine). Steps rotate over --layers distinct weight sets (default 40, 18.3 GB) and a pool of distinct tokens,
+so that no call finds its weights in the 129 MB L2. One JSON line on stdout.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs independent replicas on its own GPU (the block has no exchange step);
+value = tokens of all ranks / max elapsed over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from w4a16_top_mixture_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-block tokens/s at 2048/256x512 top-8 W4A16; achieved HBM GB/s vs peak"
+WORKLOAD = ("decode T=1: hidden 2048, 256 experts top-8 renormalised, expert intermediate 512, shared expert "
+            "intermediate 512 with sigmoid gate; int4 g64 affine experts, int8 g64 router+shared; x fp16 ~N(0,1); "
+            "uniform routing")
+SEED = 1
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record():
+    """DRAM bytes per launch from a committed ncu summary, valid only if the kernel source is unchanged."""
+    rec = os.path.join(ROOT, "profiles", "k_decode_prod_t1.json")
+    if not os.path.exists(rec):
+        return None
+    d = json.load(open(rec))
+    if d.get("kernel_src_sha256") != kernel_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w4a16_top_mixture_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(seconds=12.0, layer_seed=SEED):
+    """The float64 oracle, as it stands, on a bounded sample of the same workload (T=1 tokens through one
+    production block), single-threaded in a child process. Returns tokens/s and the sample description."""
+    code = f"""
+import os, sys, time, json
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import oracle.moe_oracle as O
+from w4a16_top_mixture_gb300 import synth
+cfg = synth.PROD
+w = synth.gen_layer(cfg, {layer_seed}, 0)
+n, t0 = 0, time.perf_counter()
+while time.perf_counter() - t0 < {seconds}:
+    x = synth.gen_token(cfg, 12345, n)[None, :]
+    O.block_forward(w, x, cfg.top_k)          # fresh dequantisation of the selected experts every token
+    n += 1
+el = time.perf_counter() - t0
+print(json.dumps({{"tokens": n, "seconds": el}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["tokens"] / d["seconds"], d
+
+
+def run_reference(args):
+    """Reference arm: the float64 oracle on the host cores, same metric/unit; each step = one token."""
+    import torch.distributed as dist  # noqa: F401
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    budget = float(os.environ.get("MOE_REF_BUDGET_S", "90"))
+    code = f"""
+import sys, time, json
+sys.path.insert(0, {ROOT!r})
+import oracle.moe_oracle as O
+from w4a16_top_mixture_gb300 import synth
+cfg = synth.PROD
+w = synth.gen_layer(cfg, {SEED}, 0)
+for i in range({args.warmup}):
+    O.block_forward(w, synth.gen_token(cfg, 999, i)[None, :], cfg.top_k)
+n, t0 = 0, time.perf_counter()
+while n < {args.steps} and (n == 0 or time.perf_counter() - t0 < {budget}):
+    O.block_forward(w, synth.gen_token(cfg, 12345, n)[None, :], cfg.top_k)
+    n += 1
+print(json.dumps({{"tokens": n, "seconds": time.perf_counter() - t0}}))
+"""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    v = d["tokens"] / d["seconds"]
+    sample = f"{d['tokens']} of {args.steps} steps timed (one token each, {budget:.0f} s budget)"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": 1},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from w4a16_top_mixture_gb300 import build, lib
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.cuda.current_device()
+    build.build()
+    cfg = synth.PROD
+    NL = args.layers
+    blocks = []
+    for l in range(NL):
+        w = synth.gen_layer(cfg, SEED + 1000 * rank, l)
+        b = lib.MoeBlock.from_config(cfg, max_tokens=1)
+        b.load_weights(w)                      # host arrays: copied and repacked by the library
+        blocks.append(b)
+        del w
+    pool = 4096
+    xh = synth.gen_x_fast(cfg, pool, 77 + rank)
+    X = torch.from_numpy(xh.view(np.int16)).cuda().view(torch.float16)
+    OUT = torch.empty_like(X)
+    st = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        b = blocks[i % NL]
+        j = i % pool
+        if ev is not None:
+            ev[0].record(st)
+        b.forward(X[j:j + 1], OUT[j:j + 1], stream=st)
+        if ev is not None:
+            ev[1].record(st)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    s, f = blocks[0].status()
+    if s != 0:
+        raise RuntimeError(f"device status {s} flags {f:#x}")
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        t_start.record(st)
+        for i in range(K):
+            step(args.warmup + i, evs[i])
+            launches += blocks[(args.warmup + i) % NL].last_launch_count()
+        t_end.record(st)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    for b in blocks[:1]:
+        s, f = b.status()
+        if s != 0:
+            raise RuntimeError(f"device status {s} flags {f:#x}")
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
+    Ke = min(K, 2000)
+    xpin = torch.from_numpy(xh[:Ke].view(np.int16).copy()).view(torch.float16).pin_memory()
+    opin = torch.empty_like(xpin).pin_memory()
+    for i in range(min(20, Ke)):
+        blocks[i % NL].forward_host(xpin[i:i + 1], opin[i:i + 1], stream=st)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        blocks[i % NL].forward_host(xpin[i:i + 1], opin[i:i + 1], stream=st)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank == 0:
+        bytes_call = synth.unique_weight_bytes(cfg, cfg.top_k)
+        peak, kind = peaks()
+        achieved = bytes_call / (kern_ms * 1e-3) / 1e9
+        tr = traffic_record()
+        cpu_v, cpu_d = cpu_baseline()
+        value = world * K / (elapsed_ms * 1e-3)
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": 1, "weight_sets": NL,
+                       "weight_bytes_resident": NL * (blocks[0].cfg.hidden and 456886400),
+                       "l2": f"inputs larger than L2: {NL} distinct weight sets rotated, a different token each step",
+                       "parallelism": f"replicas x{world}", "weights": "int4/int8 g64 affine, fp16 activations"},
+            "us_per_block": kern_ms * 1e3,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": tr, "peak_kind": kind,
+                         "algorithmic_bytes_per_launch": bytes_call,
+                         "kernel": "k_decode (fused decode kernel, one launch per step)"},
+            "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{cpu_d['tokens']} T=1 tokens through one production block in "
+                                       f"{cpu_d['seconds']:.1f} s, single-threaded float64 numpy"},
+            "e2e": {"value": world * Ke / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * cfg.hidden,
+                    "d2h_bytes_per_step": 2 * cfg.hidden,
+                    "how": "moe_block_forward_host: pinned x -> device, forward, out -> host, stream sync, per step"},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    for b in blocks:
+        b.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=40)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

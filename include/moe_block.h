@@ -1,0 +1,138 @@
+/*
+ * moe_block.h -- C ABI of the GB300 (sm_103a) W4A16 routed Mixture-of-Experts FFN block.
+ *
+ * The operation (Qwen3.6-35B-A3B decode demo on the Chimera GPNPU, section 5 "Validate the MoE FFN block",
+ * and TensorFold pull request #3239, section "Design"):
+ *
+ *   logits = W_R x               W_R: int8 group-64 affine, E expert rows stacked with the shared-gate row
+ *   p      = softmax(logits[0:E]);  S = top_k(p);  w_j = p_j / sum_{i in S} p_i        (section 5.2 ordering)
+ *   y_j    = Wd_j (silu(Wg_j x) * (Wu_j x))            routed experts, int4 group-64 affine (SwiGLU)
+ *   ys     = Wsd  (silu(Wsg x) * (Wsu x))              shared expert, int8 group-64 affine
+ *   out    = sum_{j in S} w_j y_j + sigmoid(logits[E]) * ys
+ *
+ * Activations are fp16 ("W4A16": weights int4/int8, activations fp16); every product is accumulated in fp32
+ * and the output is rounded to fp16 once. Dequantisation is w = s * q + b per group of 64 inputs, with
+ * unsigned codes and fp16 s, b.
+ *
+ * Canonical weight layout accepted by moe_block_load_weights (row-major, groups of 64 along each output row's
+ * input dimension; int4 codes two per byte, element 2c in the low nibble of byte c, element 2c+1 in the high):
+ *   router_q  [E+1][H] u8,  router_s/b  [E+1][H/64] fp16    row E is the shared-expert gate
+ *   exp_gate_q[E][I][H/2] u8, exp_gate_s/b [E][I][H/64] fp16  (exp_up_* alike)
+ *   exp_down_q[E][H][I/2] u8, exp_down_s/b [E][H][I/64] fp16
+ *   sh_gate_q [Is][H] u8,   sh_gate_s/b [Is][H/64] fp16      (sh_up_* alike)
+ *   sh_down_q [H][Is] u8,   sh_down_s/b [H][Is/64] fp16
+ *   rms_gamma [H] fp16 (stacked blocks only; NULL otherwise)
+ * fp16 values are passed as their 16-bit patterns (uint16_t).
+ *
+ * Conventions. Every entry point returns an int status (MOE_OK = 0, negative on error) and validates its
+ * arguments before touching any state; nothing throws or aborts across the ABI. Streams are cudaStream_t
+ * values passed as void* (NULL = legacy default stream). Calls on one handle must not overlap in time.
+ */
+#ifndef MOE_BLOCK_H
+#define MOE_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,     /* null / misaligned pointer, T out of range, bad index */
+  MOE_ERR_UNSUPPORTED = -2,     /* configuration has no kernel (see moe_block_create) */
+  MOE_ERR_NOT_LOADED = -3,      /* forward before load_weights */
+  MOE_ERR_CUDA = -4,            /* a CUDA runtime call failed; moe_last_cuda_error() names it */
+  MOE_ERR_DEVICE_TIMEOUT = -5,  /* a bounded device-side wait ran out (see moe_block_get_status) */
+  MOE_ERR_NO_DEVICE = -6,       /* no sm_103 device current */
+};
+
+typedef struct moe_block moe_block_t;   /* opaque, owned by the library */
+
+typedef struct {
+  int hidden;        /* H: 512, 1024 or 2048 */
+  int n_experts;     /* E: 1..512 */
+  int top_k;         /* k: 1..min(E, 16) */
+  int expert_inter;  /* I: multiple of 64, 64..1024 */
+  int shared_inter;  /* Is: multiple of 64, 64..1024 */
+  int group_size;    /* must be 64 */
+  int max_tokens;    /* largest T any forward will pass: 1..4096 (sizes the scratch allocated at create) */
+} moe_block_config_t;
+
+typedef struct {
+  const uint8_t *router_q;   const uint16_t *router_s,   *router_b;
+  const uint8_t *exp_gate_q; const uint16_t *exp_gate_s, *exp_gate_b;
+  const uint8_t *exp_up_q;   const uint16_t *exp_up_s,   *exp_up_b;
+  const uint8_t *exp_down_q; const uint16_t *exp_down_s, *exp_down_b;
+  const uint8_t *sh_gate_q;  const uint16_t *sh_gate_s,  *sh_gate_b;
+  const uint8_t *sh_up_q;    const uint16_t *sh_up_s,    *sh_up_b;
+  const uint8_t *sh_down_q;  const uint16_t *sh_down_s,  *sh_down_b;
+  const uint16_t *rms_gamma; /* may be NULL */
+} moe_block_weights_t;
+
+/* Create a handle for one block on the current CUDA device. Allocates the device weight store (repacked
+ * layout) and all scratch for max_tokens, so forward never allocates. Refuses configurations it has no
+ * kernel for with MOE_ERR_UNSUPPORTED. *out is set only on success. */
+MOE_API int moe_block_create(const moe_block_config_t *cfg, moe_block_t **out);
+
+/* Copy and repack the canonical weights into the handle. weights_on_device = 1: the pointers are device
+ * memory; 0: host memory (copied through a temporary device buffer). The caller keeps ownership and may free
+ * its buffers once this returns (the call synchronises `stream`). */
+MOE_API int moe_block_load_weights(moe_block_t *blk, const moe_block_weights_t *w, int weights_on_device, void *stream);
+
+/* out[T][H] = block(x[T][H]). x and out are caller-owned device buffers of fp16, 16-byte aligned, not
+ * aliasing. 0 <= T <= max_tokens (T = 0 is a no-op). Asynchronous on `stream`, no host synchronisation and no
+ * allocation, so it can be captured in a CUDA graph. T <= 16 runs the fused decode kernel; larger T the
+ * prompt-chunk path. */
+MOE_API int moe_block_forward(moe_block_t *blk, const void *x, void *out, int T, void *stream);
+
+/* Same computation with HOST buffers: copies x to the device, runs forward and copies out back, then
+ * synchronises `stream`. x_host/out_host should be pinned for full copy speed. */
+MOE_API int moe_block_forward_host(moe_block_t *blk, const void *x_host, void *out_host, int T, void *stream);
+
+/* Stacked configuration: h_out = h_in + block(RMSNorm(h_in)) with RMSNorm y = h / sqrt(mean(h^2) + eps) *
+ * gamma (notebook section 7: the decoder layer wraps the MoE op in RMSNorm and a residual add). Needs
+ * rms_gamma loaded. h_in and h_out fp16 device [T][H]; they may alias. */
+MOE_API int moe_block_forward_residual(moe_block_t *blk, const void *h_in, void *h_out, int T, float eps, void *stream);
+
+/* Synchronises the handle's device work and returns MOE_OK or MOE_ERR_DEVICE_TIMEOUT if a bounded
+ * device-side wait ran out in any earlier call (the handle's device state is then reset, so the next call
+ * starts clean). *flags (may be NULL) receives the raw device error bits. */
+MOE_API int moe_block_get_status(moe_block_t *blk, uint32_t *flags);
+
+MOE_API void moe_block_destroy(moe_block_t *blk);
+MOE_API const char *moe_block_strerror(int status);
+MOE_API const char *moe_last_cuda_error(void);
+
+/* ---- test hooks (not on the hot path) ---- */
+
+/* Dequantised fp32 matrix from the handle's repacked store, written to out_device (device, row-major in the
+ * canonical orientation). which: 0 router [E+1][H], 1 exp gate [I][H], 2 exp up [I][H], 3 exp down [H][I],
+ * 4 shared gate [Is][H], 5 shared up [Is][H], 6 shared down [H][Is]; index = expert for 1..3. */
+MOE_API int moe_block_debug_dequant(moe_block_t *blk, int which, int index, float *out_device, void *stream);
+
+/* Routing of the last forward call, copied to device buffers (any may be NULL): logits [T][E+1] fp32,
+ * ids [T][k] int32 ascending, weights [T][k] fp32 aligned with ids, sigmoid gate [T] fp32. */
+MOE_API int moe_block_debug_last_routing(moe_block_t *blk, int T, float *logits, int32_t *ids, float *weights,
+                                 float *sgate, void *stream);
+
+/* Test control of the bounded device waits: timeout_us = microseconds any device-side wait may last before
+ * it gives up (0 = the default, 500 ms); skip_arrive = 1 makes CTA 0 withhold its logits arrival in the next
+ * forward call only, so every CTA's bounded wait for the logits runs out and the call ends early with an
+ * error bit set (the host then sees MOE_ERR_DEVICE_TIMEOUT from moe_block_get_status). */
+MOE_API int moe_block_debug_set_wait(moe_block_t *blk, uint32_t timeout_us, int skip_arrive);
+
+/* Number of CUDA kernel launches the last forward call made. */
+MOE_API int moe_block_last_launch_count(moe_block_t *blk);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_BLOCK_H */

@@ -1,0 +1,53 @@
+"""Seeded test workloads: synth draws the inputs; the oracle's exact float64 router logits decide which
+tokens to redraw so that every token's k-th/(k+1)-th expert-logit gap is at least 1e-2 (the block
+specification's rule for bit-exact expert ids; routing flips below a 0.015 gap are the failure mode the
+TensorFold pull request #3239 reports under "Receipts")."""
+import numpy as np
+
+import oracle.moe_oracle as O
+from w4a16_top_mixture_gb300 import synth
+
+MIN_GAP = 1e-2
+
+
+def gaps(logits_e, k):
+    s = -np.sort(-logits_e, axis=-1)
+    return s[:, k - 1] - s[:, k]
+
+
+def make_case(cfg, T, seed, routing="uniform", layer=0, max_iter=64):
+    w = synth.gen_layer(cfg, seed, layer)
+    attempts = {}
+    x = synth.gen_x(cfg, T, seed, attempts=attempts)
+    for _ in range(max_iter):
+        if routing == "zipf":
+            w["router_q"], w["router_s"], w["router_b"] = synth.zipf_router(cfg, x, seed, layer,
+                                                                             attempt=sum(attempts.values()))
+        Wr = O.dequant_int8(w["router_q"], w["router_s"], w["router_b"])
+        lg = x.astype(np.float64) @ Wr.T
+        bad = np.nonzero(gaps(lg[:, :cfg.n_experts], cfg.top_k) < MIN_GAP)[0]
+        if len(bad) == 0:
+            return w, x
+        for t in bad:
+            attempts[int(t)] = attempts.get(int(t), 0) + 1
+            x[t] = synth.gen_token(cfg, seed, int(t), attempts[int(t)])
+    raise RuntimeError("could not draw a gap-respecting case")
+
+
+def rel_err(out_gpu, out_ref):
+    """max |err| / RMS(out_ref) over the whole output."""
+    ref = np.asarray(out_ref, np.float64)
+    err = np.abs(np.asarray(out_gpu, np.float64) - ref).max()
+    return err / np.sqrt(np.mean(ref * ref))
+
+
+def structural(out_gpu, r):
+    """The block gates of the Chimera notebook (section 5 summary): cosine, norm ratio and the shared branch's
+    share of the move away from the routed half."""
+    g = np.asarray(out_gpu, np.float64).ravel()
+    ref = r["out"].ravel()
+    cos = float(g @ ref / (np.linalg.norm(g) * np.linalg.norm(ref)))
+    ratio = float(np.linalg.norm(g) / np.linalg.norm(ref))
+    routed = r["routed"].ravel()
+    moved = np.linalg.norm(g - routed) / np.linalg.norm(ref - routed)
+    return cos, ratio, moved

@@ -1,0 +1,319 @@
+// C ABI of the block (declared in include/moe_block.h): argument validation, device memory, weight loading
+// and dispatch to the kernels. No call throws or aborts; every failure is a negative status.
+#include <cuda_runtime.h>
+#include <new>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/moe_block.h"
+#include "decode.cuh"
+#include "layout.cuh"
+#include "repack.cuh"
+
+using namespace moe;
+
+struct moe_block {
+  moe_block_config_t cfg;
+  MoeLayout L;
+  int dev = 0, num_sms = 0, max_smem = 0;
+  uint8_t* wstore = nullptr;                       // one allocation for all repacked weights
+  uint8_t *router = nullptr, *sh_gu = nullptr, *sh_dn = nullptr, *ex_gu = nullptr, *ex_dn = nullptr;
+  uint16_t* gamma = nullptr;
+  bool loaded = false, has_gamma = false;
+  int dec_T = 0;                                   // largest T the decode scratch holds
+  float *logits = nullptr, *hs = nullptr, *partial = nullptr;
+  uint32_t *counters = nullptr, *status = nullptr;
+  int32_t* rec_ids = nullptr;
+  float *rec_w = nullptr, *rec_sg = nullptr;
+  uint16_t *xbuf = nullptr, *obuf = nullptr;       // staging for forward_host
+  uint64_t timeout_ns = 500ull * 1000 * 1000;
+  int skip_arrive = 0;
+  int last_launches = 0;
+  int last_T = 0;
+};
+
+static thread_local char g_cuda_err[256] = "";
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", what, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+#define CK(call)                                        \
+  do {                                                  \
+    cudaError_t _e = (call);                            \
+    if (_e != cudaSuccess) return cuda_fail(_e, #call); \
+  } while (0)
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+extern "C" const char* moe_last_cuda_error(void) { return g_cuda_err; }
+
+extern "C" const char* moe_block_strerror(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_NOT_LOADED: return "weights not loaded";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+    case MOE_ERR_NO_DEVICE: return "no sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+static void free_all(moe_block* b) {
+  cudaFree(b->wstore);
+  cudaFree(b->gamma);
+  cudaFree(b->logits);
+  cudaFree(b->hs);
+  cudaFree(b->partial);
+  cudaFree(b->counters);
+  cudaFree(b->rec_ids);
+  cudaFree(b->rec_w);
+  cudaFree(b->rec_sg);
+  cudaFree(b->xbuf);
+  cudaFree(b->obuf);
+}
+
+extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out) {
+  if (!cfg || !out) return MOE_ERR_INVALID_ARG;
+  const moe_block_config_t c = *cfg;
+  if (c.group_size != 64) return MOE_ERR_UNSUPPORTED;
+  if (c.hidden != 512 && c.hidden != 1024 && c.hidden != 2048) return MOE_ERR_UNSUPPORTED;
+  if (c.n_experts < 1 || c.n_experts > 512) return MOE_ERR_UNSUPPORTED;
+  if (c.top_k < 1 || c.top_k > 16 || c.top_k > c.n_experts) return MOE_ERR_UNSUPPORTED;
+  if (c.expert_inter < 64 || c.expert_inter > 1024 || c.expert_inter % 64) return MOE_ERR_UNSUPPORTED;
+  if (c.shared_inter < 64 || c.shared_inter > 1024 || c.shared_inter % 64) return MOE_ERR_UNSUPPORTED;
+  if (c.max_tokens < 1 || c.max_tokens > 4096) return MOE_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_NO_DEVICE;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_NO_DEVICE;
+  if (prop.major != 10 || prop.minor != 3) {
+    snprintf(g_cuda_err, sizeof(g_cuda_err), "device is sm_%d%d, library is built for sm_103a", prop.major,
+             prop.minor);
+    return MOE_ERR_NO_DEVICE;
+  }
+  moe_block* b = new (std::nothrow) moe_block;
+  if (!b) return MOE_ERR_CUDA;
+  b->cfg = c;
+  b->L = moe_make_layout(c.hidden, c.n_experts, c.top_k, c.expert_inter, c.shared_inter);
+  b->dev = dev;
+  b->num_sms = prop.multiProcessorCount;
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  b->max_smem = optin;
+  // the decode kernel needs a plan for every T it may see
+  b->dec_T = c.max_tokens < DEC_TMAX ? c.max_tokens : DEC_TMAX;
+  for (int T = 1; T <= b->dec_T; ++T) {
+    DecodeLaunch pl;
+    if (!decode_plan(b->L, T, b->num_sms, b->max_smem, &pl)) { delete b; return MOE_ERR_UNSUPPORTED; }
+  }
+  const MoeLayout& L = b->L;
+  size_t total = L.router_bytes + L.shgu_bytes + L.shdn_bytes + L.exgu_bytes + L.exdn_bytes;
+  cudaError_t e = cudaMalloc(&b->wstore, total);
+  if (e == cudaSuccess) {
+    b->router = b->wstore;
+    b->sh_gu = b->router + L.router_bytes;
+    b->sh_dn = b->sh_gu + L.shgu_bytes;
+    b->ex_gu = b->sh_dn + L.shdn_bytes;
+    b->ex_dn = b->ex_gu + L.exgu_bytes;
+  }
+  const int T = b->dec_T;
+  if (e == cudaSuccess) e = cudaMalloc(&b->gamma, (size_t)c.hidden * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&b->logits, (size_t)T * (c.n_experts + 1) * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->hs, (size_t)T * c.shared_inter * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->partial, decode_partial_floats(L, b->num_sms, T) * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->counters, 8 * 4);
+  if (e == cudaSuccess) e = cudaMemset(b->counters, 0, 8 * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->rec_ids, (size_t)T * c.top_k * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->rec_w, (size_t)T * c.top_k * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->rec_sg, (size_t)T * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->xbuf, (size_t)c.max_tokens * c.hidden * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&b->obuf, (size_t)c.max_tokens * c.hidden * 2);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_all(b);
+    delete b;
+    return cuda_fail(e, "moe_block_create");
+  }
+  b->status = b->counters + 4;
+  *out = b;
+  return MOE_OK;
+}
+
+extern "C" void moe_block_destroy(moe_block_t* b) {
+  if (!b) return;
+  cudaDeviceSynchronize();
+  free_all(b);
+  delete b;
+}
+
+extern "C" int moe_block_load_weights(moe_block_t* b, const moe_block_weights_t* w, int on_device, void* stream) {
+  if (!b || !w) return MOE_ERR_INVALID_ARG;
+  const void* req[] = {w->router_q, w->router_s, w->router_b, w->exp_gate_q, w->exp_gate_s, w->exp_gate_b,
+                       w->exp_up_q, w->exp_up_s, w->exp_up_b, w->exp_down_q, w->exp_down_s, w->exp_down_b,
+                       w->sh_gate_q, w->sh_gate_s, w->sh_gate_b, w->sh_up_q, w->sh_up_s, w->sh_up_b,
+                       w->sh_down_q, w->sh_down_s, w->sh_down_b};
+  for (const void* p : req)
+    if (!p) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const moe_block_config_t& c = b->cfg;
+  const size_t H = c.hidden, E = c.n_experts, I = c.expert_inter, Is = c.shared_inter;
+  // sizes in bytes of the 21 canonical arrays, in the order of `req`
+  const size_t sz[] = {(E + 1) * H, (E + 1) * (H / 64) * 2, (E + 1) * (H / 64) * 2,
+                       E * I * H / 2, E * I * (H / 64) * 2, E * I * (H / 64) * 2,
+                       E * I * H / 2, E * I * (H / 64) * 2, E * I * (H / 64) * 2,
+                       E * H * I / 2, E * H * (I / 64) * 2, E * H * (I / 64) * 2,
+                       Is * H, Is * (H / 64) * 2, Is * (H / 64) * 2,
+                       Is * H, Is * (H / 64) * 2, Is * (H / 64) * 2,
+                       H * Is, H * (Is / 64) * 2, H * (Is / 64) * 2};
+  const void* dptr[21];
+  uint8_t* tmp = nullptr;
+  if (on_device) {
+    for (int i = 0; i < 21; ++i) dptr[i] = req[i];
+  } else {
+    size_t total = 0;
+    for (size_t s : sz) total += (s + 255) & ~(size_t)255;
+    CK(cudaMalloc(&tmp, total));
+    size_t off = 0;
+    for (int i = 0; i < 21; ++i) {
+      cudaError_t e = cudaMemcpyAsync(tmp + off, req[i], sz[i], cudaMemcpyHostToDevice, st);
+      if (e != cudaSuccess) { cudaFree(tmp); return cuda_fail(e, "load_weights copy"); }
+      dptr[i] = tmp + off;
+      off += (sz[i] + 255) & ~(size_t)255;
+    }
+  }
+  RepackSrc src;
+  src.router_q = (const uint8_t*)dptr[0]; src.router_s = (const uint16_t*)dptr[1]; src.router_b = (const uint16_t*)dptr[2];
+  src.exp_gate_q = (const uint8_t*)dptr[3]; src.exp_gate_s = (const uint16_t*)dptr[4]; src.exp_gate_b = (const uint16_t*)dptr[5];
+  src.exp_up_q = (const uint8_t*)dptr[6]; src.exp_up_s = (const uint16_t*)dptr[7]; src.exp_up_b = (const uint16_t*)dptr[8];
+  src.exp_down_q = (const uint8_t*)dptr[9]; src.exp_down_s = (const uint16_t*)dptr[10]; src.exp_down_b = (const uint16_t*)dptr[11];
+  src.sh_gate_q = (const uint8_t*)dptr[12]; src.sh_gate_s = (const uint16_t*)dptr[13]; src.sh_gate_b = (const uint16_t*)dptr[14];
+  src.sh_up_q = (const uint8_t*)dptr[15]; src.sh_up_s = (const uint16_t*)dptr[16]; src.sh_up_b = (const uint16_t*)dptr[17];
+  src.sh_down_q = (const uint8_t*)dptr[18]; src.sh_down_s = (const uint16_t*)dptr[19]; src.sh_down_b = (const uint16_t*)dptr[20];
+  RepackDst dst{b->router, b->sh_gu, b->sh_dn, b->ex_gu, b->ex_dn};
+  cudaError_t e = repack_all(src, b->L, dst, st);
+  if (e == cudaSuccess && w->rms_gamma) {
+    e = cudaMemcpyAsync(b->gamma, w->rms_gamma, H * 2, on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                        st);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (tmp) cudaFree(tmp);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_block_load_weights");
+  b->has_gamma = w->rms_gamma != nullptr;
+  b->loaded = true;
+  return MOE_OK;
+}
+
+static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, const uint16_t* gamma, float eps,
+                       cudaStream_t st) {
+  b->last_launches = 0;
+  b->last_T = T;
+  for (int t0 = 0; t0 < T; t0 += DEC_TMAX) {
+    const int n = T - t0 < DEC_TMAX ? T - t0 : DEC_TMAX;
+    DecodeLaunch pl;
+    if (!decode_plan(b->L, n, b->num_sms, b->max_smem, &pl)) return MOE_ERR_UNSUPPORTED;
+    DecodeArgs a;
+    a.router = b->router; a.sh_gu = b->sh_gu; a.sh_dn = b->sh_dn; a.ex_gu = b->ex_gu; a.ex_dn = b->ex_dn;
+    a.x = x + (size_t)t0 * b->cfg.hidden;
+    a.out = out + (size_t)t0 * b->cfg.hidden;
+    a.gamma = gamma;
+    a.eps = eps;
+    a.T = n;
+    a.logits = b->logits; a.hs = b->hs; a.partial = b->partial;
+    a.counters = b->counters; a.status = b->status;
+    a.rec_ids = b->rec_ids; a.rec_w = b->rec_w; a.rec_sg = b->rec_sg;
+    a.timeout_ns = b->timeout_ns;
+    a.skip_arrive = b->skip_arrive;
+    b->skip_arrive = 0;
+    cudaError_t e = decode_launch(b->L, a, pl, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    ++b->last_launches;
+  }
+  return MOE_OK;
+}
+
+extern "C" int moe_block_forward(moe_block_t* b, const void* x, void* out, int T, void* stream) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > b->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) { b->last_launches = 0; return MOE_OK; }
+  if (!x || !out || !aligned16(x) || !aligned16(out) || x == out) return MOE_ERR_INVALID_ARG;
+  if (!b->loaded) return MOE_ERR_NOT_LOADED;
+  return run_forward(b, (const uint16_t*)x, (uint16_t*)out, T, nullptr, 0.f, (cudaStream_t)stream);
+}
+
+extern "C" int moe_block_forward_residual(moe_block_t* b, const void* h_in, void* h_out, int T, float eps,
+                                          void* stream) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > b->cfg.max_tokens || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) { b->last_launches = 0; return MOE_OK; }
+  if (!h_in || !h_out || !aligned16(h_in) || !aligned16(h_out)) return MOE_ERR_INVALID_ARG;
+  if (!b->loaded) return MOE_ERR_NOT_LOADED;
+  if (!b->has_gamma) return MOE_ERR_NOT_LOADED;
+  if (T > DEC_TMAX && h_in == h_out) return MOE_ERR_INVALID_ARG;
+  return run_forward(b, (const uint16_t*)h_in, (uint16_t*)h_out, T, b->gamma, eps, (cudaStream_t)stream);
+}
+
+extern "C" int moe_block_forward_host(moe_block_t* b, const void* x_host, void* out_host, int T, void* stream) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > b->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (!b->loaded) return MOE_ERR_NOT_LOADED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t bytes = (size_t)T * b->cfg.hidden * 2;
+  CK(cudaMemcpyAsync(b->xbuf, x_host, bytes, cudaMemcpyHostToDevice, st));
+  int s = run_forward(b, b->xbuf, b->obuf, T, nullptr, 0.f, st);
+  if (s != MOE_OK) return s;
+  CK(cudaMemcpyAsync(out_host, b->obuf, bytes, cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  return MOE_OK;
+}
+
+extern "C" int moe_block_get_status(moe_block_t* b, uint32_t* flags) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  CK(cudaDeviceSynchronize());
+  uint32_t st = 0;
+  CK(cudaMemcpy(&st, b->status, 4, cudaMemcpyDeviceToHost));
+  if (flags) *flags = st;
+  if (st) {
+    CK(cudaMemset(b->counters, 0, 8 * 4));
+    CK(cudaDeviceSynchronize());
+    return MOE_ERR_DEVICE_TIMEOUT;
+  }
+  return MOE_OK;
+}
+
+extern "C" int moe_block_debug_dequant(moe_block_t* b, int which, int index, float* out, void* stream) {
+  if (!b || !out || which < 0 || which > 6) return MOE_ERR_INVALID_ARG;
+  if (!b->loaded) return MOE_ERR_NOT_LOADED;
+  if (which >= 1 && which <= 3 && (index < 0 || index >= b->cfg.n_experts)) return MOE_ERR_INVALID_ARG;
+  const uint8_t* base = which == 0 ? b->router : which <= 2 ? b->ex_gu : which == 3 ? b->ex_dn
+                      : which <= 5 ? b->sh_gu : b->sh_dn;
+  cudaError_t e = debug_dequant(base, b->L, which, index, out, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "debug_dequant");
+  return MOE_OK;
+}
+
+extern "C" int moe_block_debug_last_routing(moe_block_t* b, int T, float* logits, int32_t* ids, float* w,
+                                            float* sg, void* stream) {
+  if (!b || T < 1 || T > b->dec_T || T > b->last_T) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int E = b->cfg.n_experts, K = b->cfg.top_k;
+  if (logits) CK(cudaMemcpyAsync(logits, b->logits, (size_t)T * (E + 1) * 4, cudaMemcpyDeviceToDevice, st));
+  if (ids) CK(cudaMemcpyAsync(ids, b->rec_ids, (size_t)T * K * 4, cudaMemcpyDeviceToDevice, st));
+  if (w) CK(cudaMemcpyAsync(w, b->rec_w, (size_t)T * K * 4, cudaMemcpyDeviceToDevice, st));
+  if (sg) CK(cudaMemcpyAsync(sg, b->rec_sg, (size_t)T * 4, cudaMemcpyDeviceToDevice, st));
+  return MOE_OK;
+}
+
+extern "C" int moe_block_debug_set_wait(moe_block_t* b, uint32_t timeout_us, int skip_arrive) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  b->timeout_ns = timeout_us ? (uint64_t)timeout_us * 1000ull : 500ull * 1000 * 1000;
+  b->skip_arrive = skip_arrive ? 1 : 0;
+  return MOE_OK;
+}
+
+extern "C" int moe_block_last_launch_count(moe_block_t* b) { return b ? b->last_launches : 0; }

@@ -1,0 +1,49 @@
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "layout.cuh"
+
+namespace moe {
+
+constexpr int DEC_NCW = 16;                       // consumer warps
+constexpr int DEC_THREADS = (DEC_NCW + 1) * 32;   // + one producer warp
+constexpr int DEC_TMAX = 16;                      // largest T of the fused decode kernel
+constexpr int DEC_MAXSEG = 4;                     // expert segments one CTA's unit range may touch
+constexpr int DEC_MAXNS = 24;                     // ring stages
+
+// device error bits
+enum : uint32_t {
+  ERR_WAIT_LOGITS = 1u, ERR_WAIT_HS = 2u, ERR_WAIT_PARTIAL = 4u, ERR_WAIT_FULL = 8u, ERR_WAIT_EMPTY = 16u,
+  ERR_WAIT_ROUTE = 32u, ERR_SEGMENTS = 64u, ERR_HSEG = 128u,
+};
+
+struct DecodeArgs {
+  const uint8_t *router, *sh_gu, *sh_dn, *ex_gu, *ex_dn;
+  const uint16_t* x;        // [T][H] fp16 (h_in in residual mode)
+  uint16_t* out;            // [T][H] fp16
+  const uint16_t* gamma;    // non-null: residual mode, x_hat = RMSNorm(x), out = x + block(x_hat)
+  float eps;
+  int T;
+  float* logits;            // [T][E+1]
+  float* hs;                // [T][Is]
+  float* partial;           // [G*MAXSEG*T][H]
+  uint32_t* counters;       // [4]
+  uint32_t* status;
+  int32_t* rec_ids;         // routing record [T][K] (written by CTA 0)
+  float* rec_w;             // [T][K]
+  float* rec_sg;            // [T]
+  uint64_t timeout_ns;
+  int skip_arrive;
+};
+
+struct DecodeLaunch {
+  int grid, smem, NS, SS, hseg_floats;
+};
+
+// Host: shared-memory plan for a call with T tokens; returns false if it does not fit.
+bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch* out);
+cudaError_t decode_launch(const MoeLayout& L, const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st);
+size_t decode_partial_floats(const MoeLayout& L, int grid, int T);
+
+}  // namespace moe

@@ -1,0 +1,67 @@
+// Device-resident (repacked) layout of one block's weights, shared by the repack, debug and forward kernels.
+//
+// The canonical layout (see include/moe_block.h) is regrouped at load time so that every unit of work a CTA
+// streams is one contiguous, 16-byte aligned range that a single bulk copy can move into shared memory:
+//
+//   router   [E+1][RR]     row r: int8 codes of the row, permuted (see int8_perm), then H/64 (s,b) fp16 pairs
+//   sh_gu    [Is][SU]      unit i: gate row codes (permuted) | up row codes (permuted) | gate (s,b) | up (s,b)
+//   sh_dn    [H][SDR]      row r: Is int8 codes in natural order | Is/64 (s,b)
+//   ex_gu    [E][I][EU]    unit (e,i): gate row int4 codes | up row int4 codes | gate (s,b) | up (s,b)
+//   ex_dn    [E][I/64][DB] per (expert, group of 64 intermediate units): (s,b) of every output row (H pairs),
+//                          then 64 units, each the unit's COLUMN of the down matrix as H int4 codes, two per
+//                          byte (row 2m in the low nibble of byte m)
+//
+// Row codes of int4 matrices keep the canonical packing. int8 rows are permuted in 16-byte blocks so that the
+// lanes of a warp read consecutive 16 bytes: the 32-column chunk c = l + LW*p, half h (16 columns), lands at
+// byte ((p*2 + h)*LW + l)*16 of the row, where LW = min(32, H/32) lanes work on a row.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef MOE_HD
+#ifdef __CUDACC__
+#define MOE_HD __host__ __device__ __forceinline__
+#else
+#define MOE_HD inline
+#endif
+#endif
+
+MOE_HD size_t moe_align16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+struct MoeLayout {
+  int H, E, K, I, Is;
+  int GB, GI, GS;     // groups of 64 along H, I, Is
+  int NCH, LW, P;     // 32-column chunks per H row, lanes per row, chunks per lane
+  size_t RR, SU, SDR, EU, DSB, DCB, DB;
+  size_t router_bytes, shgu_bytes, shdn_bytes, exgu_bytes, exdn_bytes;
+  size_t exgu_expert, exdn_expert;
+};
+
+inline MoeLayout moe_make_layout(int H, int E, int K, int I, int Is) {
+  MoeLayout L;
+  L.H = H; L.E = E; L.K = K; L.I = I; L.Is = Is;
+  L.GB = H / 64; L.GI = I / 64; L.GS = Is / 64;
+  L.NCH = H / 32; L.LW = L.NCH < 32 ? L.NCH : 32; L.P = (L.NCH + 31) / 32;
+  L.RR = moe_align16((size_t)H + (size_t)L.GB * 4);
+  L.SU = moe_align16(2 * (size_t)H + 2 * (size_t)L.GB * 4);
+  L.SDR = moe_align16((size_t)Is + (size_t)L.GS * 4);
+  L.EU = moe_align16((size_t)H + 2 * (size_t)L.GB * 4);
+  L.DSB = (size_t)H * 4;
+  L.DCB = (size_t)H / 2;
+  L.DB = L.DSB + 64 * L.DCB;
+  L.router_bytes = (size_t)(E + 1) * L.RR;
+  L.shgu_bytes = (size_t)Is * L.SU;
+  L.shdn_bytes = (size_t)H * L.SDR;
+  L.exgu_expert = (size_t)I * L.EU;
+  L.exdn_expert = (size_t)L.GI * L.DB;
+  L.exgu_bytes = (size_t)E * L.exgu_expert;
+  L.exdn_bytes = (size_t)E * L.exdn_expert;
+  return L;
+}
+
+// byte position of int8 column j inside a permuted row
+MOE_HD int moe_int8_perm(int j, int LW) {
+  int c = j >> 5, within = j & 31, h = within >> 4, b = within & 15;
+  int l = c % LW, p = c / LW;
+  return ((p * 2 + h) * LW + l) * 16 + b;
+}

@@ -1,0 +1,227 @@
+"""ctypes binding of libmoeblock.so (include/moe_block.h). Argument marshalling only: every step of the block
+runs in the library's CUDA kernels; torch supplies device memory and streams. A missing library raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoeblock.so")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_NOT_LOADED",
+          -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT", -6: "MOE_ERR_NO_DEVICE"}
+
+WEIGHT_FIELDS = [
+    "router_q", "router_s", "router_b", "exp_gate_q", "exp_gate_s", "exp_gate_b", "exp_up_q", "exp_up_s",
+    "exp_up_b", "exp_down_q", "exp_down_s", "exp_down_b", "sh_gate_q", "sh_gate_s", "sh_gate_b", "sh_up_q",
+    "sh_up_s", "sh_up_b", "sh_down_q", "sh_down_s", "sh_down_b", "rms_gamma",
+]
+EXPORTS = ["moe_block_create", "moe_block_load_weights", "moe_block_forward", "moe_block_forward_host",
+           "moe_block_forward_residual", "moe_block_get_status", "moe_block_destroy", "moe_block_strerror",
+           "moe_last_cuda_error", "moe_block_debug_dequant", "moe_block_debug_last_routing",
+           "moe_block_debug_set_wait", "moe_block_last_launch_count"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        lib = _LIB
+        extra = ""
+        if lib is not None and status == -4:
+            extra = " (" + lib.moe_last_cuda_error().decode() + ")"
+        super().__init__(f"{what}: {STATUS.get(status, status)}{extra}")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("expert_inter", ctypes.c_int), ("shared_inter", ctypes.c_int), ("group_size", ctypes.c_int),
+                ("max_tokens", ctypes.c_int)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+_LIB = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libmoeblock.so (built by w4a16_top_mixture_gb300.build). Raises if it is missing."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m w4a16_top_mixture_gb300.build` "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    vp, i, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32
+    lib.moe_block_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(vp)]
+    lib.moe_block_load_weights.argtypes = [vp, ctypes.POINTER(Weights), i, vp]
+    lib.moe_block_forward.argtypes = [vp, vp, vp, i, vp]
+    lib.moe_block_forward_host.argtypes = [vp, vp, vp, i, vp]
+    lib.moe_block_forward_residual.argtypes = [vp, vp, vp, i, ctypes.c_float, vp]
+    lib.moe_block_get_status.argtypes = [vp, ctypes.POINTER(u32)]
+    lib.moe_block_destroy.argtypes = [vp]
+    lib.moe_block_destroy.restype = None
+    lib.moe_block_strerror.argtypes = [i]
+    lib.moe_block_strerror.restype = ctypes.c_char_p
+    lib.moe_last_cuda_error.argtypes = []
+    lib.moe_last_cuda_error.restype = ctypes.c_char_p
+    lib.moe_block_debug_dequant.argtypes = [vp, i, i, vp, vp]
+    lib.moe_block_debug_last_routing.argtypes = [vp, i, vp, vp, vp, vp, vp]
+    lib.moe_block_debug_set_wait.argtypes = [vp, u32, i]
+    lib.moe_block_last_launch_count.argtypes = [vp]
+    for n in EXPORTS:
+        if not hasattr(lib, n):
+            raise RuntimeError(f"{path} does not export {n}")
+    _LIB = lib
+    return lib
+
+
+def _check(status, what):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+class MoeBlock:
+    """One block's weights on the current CUDA device, and its forward entry points."""
+
+    def __init__(self, hidden=2048, n_experts=256, top_k=8, expert_inter=512, shared_inter=512, max_tokens=16):
+        self.lib = load_library()
+        self.cfg = Config(hidden, n_experts, top_k, expert_inter, shared_inter, 64, max_tokens)
+        h = ctypes.c_void_p()
+        _check(self.lib.moe_block_create(ctypes.byref(self.cfg), ctypes.byref(h)), "moe_block_create")
+        self.h = h
+        self.hidden, self.n_experts, self.top_k = hidden, n_experts, top_k
+        self.max_tokens = max_tokens
+
+    @classmethod
+    def from_config(cls, cfg, max_tokens=16):
+        return cls(cfg.hidden, cfg.n_experts, cfg.top_k, cfg.expert_inter, cfg.shared_inter, max_tokens)
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.moe_block_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def load_weights(self, w: dict, stream=None):
+        """w: canonical arrays (numpy on the host, or torch tensors on the device; fp16 as float16/uint16)."""
+        import torch
+        keep = []
+        on_dev = None
+        W = Weights()
+        for n in WEIGHT_FIELDS:
+            a = w.get(n)
+            if a is None:
+                continue
+            if isinstance(a, np.ndarray):
+                a = np.ascontiguousarray(a)
+                if on_dev is None:
+                    on_dev = False
+                if on_dev:
+                    raise ValueError("mix of host and device weights")
+                keep.append(a)
+                setattr(W, n, a.ctypes.data)
+            else:
+                assert isinstance(a, torch.Tensor) and a.is_cuda and a.is_contiguous()
+                if on_dev is None:
+                    on_dev = True
+                if not on_dev:
+                    raise ValueError("mix of host and device weights")
+                keep.append(a)
+                setattr(W, n, a.data_ptr())
+        _check(self.lib.moe_block_load_weights(self.h, ctypes.byref(W), int(bool(on_dev)), _stream_ptr(stream)),
+               "moe_block_load_weights")
+
+    def forward(self, x, out=None, stream=None):
+        import torch
+        assert x.dtype == torch.float16 and x.is_cuda and x.is_contiguous()
+        if out is None:
+            out = torch.empty_like(x)
+        T = x.shape[0] if x.dim() == 2 else 0
+        _check(self.lib.moe_block_forward(self.h, _ptr(x), _ptr(out), T, _stream_ptr(stream)), "moe_block_forward")
+        return out
+
+    def forward_residual(self, h_in, h_out=None, eps=1e-6, stream=None):
+        import torch
+        assert h_in.dtype == torch.float16 and h_in.is_cuda and h_in.is_contiguous()
+        if h_out is None:
+            h_out = torch.empty_like(h_in)
+        _check(self.lib.moe_block_forward_residual(self.h, _ptr(h_in), _ptr(h_out), h_in.shape[0], float(eps),
+                                                   _stream_ptr(stream)), "moe_block_forward_residual")
+        return h_out
+
+    def forward_host(self, x_host, out_host=None, stream=None):
+        """x_host: numpy/pinned-torch fp16 [T, H] on the host; returns the host output."""
+        import torch
+        if isinstance(x_host, np.ndarray):
+            x_host = torch.from_numpy(np.ascontiguousarray(x_host))
+        if out_host is None:
+            out_host = torch.empty_like(x_host)
+        _check(self.lib.moe_block_forward_host(self.h, _ptr(x_host), _ptr(out_host), x_host.shape[0],
+                                               _stream_ptr(stream)), "moe_block_forward_host")
+        return out_host
+
+    def status(self):
+        f = ctypes.c_uint32(0)
+        s = self.lib.moe_block_get_status(self.h, ctypes.byref(f))
+        return s, f.value
+
+    def debug_dequant(self, which, index=0, stream=None):
+        import torch
+        H, E, I, Is = self.cfg.hidden, self.cfg.n_experts, self.cfg.expert_inter, self.cfg.shared_inter
+        shape = {0: (E + 1, H), 1: (I, H), 2: (I, H), 3: (H, I), 4: (Is, H), 5: (Is, H), 6: (H, Is)}[which]
+        out = torch.empty(shape, dtype=torch.float32, device="cuda")
+        _check(self.lib.moe_block_debug_dequant(self.h, which, index, _ptr(out), _stream_ptr(stream)),
+               "moe_block_debug_dequant")
+        return out
+
+    def last_routing(self, T, stream=None):
+        import torch
+        E, K = self.cfg.n_experts, self.cfg.top_k
+        lg = torch.empty((T, E + 1), dtype=torch.float32, device="cuda")
+        ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        sg = torch.empty((T,), dtype=torch.float32, device="cuda")
+        _check(self.lib.moe_block_debug_last_routing(self.h, T, _ptr(lg), _ptr(ids), _ptr(w), _ptr(sg),
+                                                     _stream_ptr(stream)), "moe_block_debug_last_routing")
+        return {"logits": lg, "ids": ids, "w": w, "sg": sg}
+
+    def set_wait(self, timeout_us=0, skip_arrive=False):
+        _check(self.lib.moe_block_debug_set_wait(self.h, int(timeout_us), int(bool(skip_arrive))), "set_wait")
+
+    def last_launch_count(self):
+        return self.lib.moe_block_last_launch_count(self.h)
+
+
+def upload_weights(w: dict, device="cuda"):
+    """Canonical numpy arrays -> contiguous torch tensors on the device (fp16 arrays as uint16 bit patterns)."""
+    import torch
+    out = {}
+    for k, v in w.items():
+        a = np.ascontiguousarray(v)
+        if a.dtype == np.float16:
+            a = a.view(np.int16)          # bit patterns; the library reads them as fp16
+        elif a.dtype == np.uint8:
+            pass
+        out[k] = torch.from_numpy(a).to(device)
+    return out
