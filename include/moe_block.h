@@ -129,6 +129,11 @@ MOE_API int moe_block_debug_last_routing(moe_block_t *blk, int T, float *logits,
  * error bit set (the host then sees MOE_ERR_DEVICE_TIMEOUT from moe_block_get_status). */
 MOE_API int moe_block_debug_set_wait(moe_block_t *blk, uint32_t timeout_us, int skip_arrive);
 
+/* Phase timestamps for performance analysis: when trace_device is non-NULL, every later decode call writes
+ * %globaltimer nanosecond stamps at its phase boundaries into trace_device[cta * 32 + slot] (uint64, device
+ * memory of at least 32 * number-of-SMs entries, caller-owned); NULL switches tracing off. */
+MOE_API int moe_block_debug_set_trace(moe_block_t *blk, void *trace_device);
+
 /* Number of CUDA kernel launches the last forward call made. */
 MOE_API int moe_block_last_launch_count(moe_block_t *blk);
 

@@ -31,6 +31,8 @@ struct moe_block {
   int skip_arrive = 0;
   int last_launches = 0;
   int last_T = 0;
+  DecodeLaunch plans[DEC_TMAX + 1];                // launch plan per T, computed at create
+  uint64_t* trace = nullptr;                       // optional phase-timestamp buffer (debug)
 };
 
 static thread_local char g_cuda_err[256] = "";
@@ -105,10 +107,10 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   b->max_smem = optin;
   // the decode kernel needs a plan for every T it may see
+  if (!decode_supported(b->L)) { delete b; return MOE_ERR_UNSUPPORTED; }
   b->dec_T = c.max_tokens < DEC_TMAX ? c.max_tokens : DEC_TMAX;
   for (int T = 1; T <= b->dec_T; ++T) {
-    DecodeLaunch pl;
-    if (!decode_plan(b->L, T, b->num_sms, b->max_smem, &pl)) { delete b; return MOE_ERR_UNSUPPORTED; }
+    if (!decode_plan(b->L, T, b->num_sms, b->max_smem, &b->plans[T])) { delete b; return MOE_ERR_UNSUPPORTED; }
   }
   const MoeLayout& L = b->L;
   size_t total = L.router_bytes + L.shgu_bytes + L.shdn_bytes + L.exgu_bytes + L.exdn_bytes;
@@ -213,8 +215,7 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
   b->last_T = T;
   for (int t0 = 0; t0 < T; t0 += DEC_TMAX) {
     const int n = T - t0 < DEC_TMAX ? T - t0 : DEC_TMAX;
-    DecodeLaunch pl;
-    if (!decode_plan(b->L, n, b->num_sms, b->max_smem, &pl)) return MOE_ERR_UNSUPPORTED;
+    const DecodeLaunch& pl = b->plans[n];
     DecodeArgs a;
     a.router = b->router; a.sh_gu = b->sh_gu; a.sh_dn = b->sh_dn; a.ex_gu = b->ex_gu; a.ex_dn = b->ex_dn;
     a.x = x + (size_t)t0 * b->cfg.hidden;
@@ -227,6 +228,7 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
     a.rec_ids = b->rec_ids; a.rec_w = b->rec_w; a.rec_sg = b->rec_sg;
     a.timeout_ns = b->timeout_ns;
     a.skip_arrive = b->skip_arrive;
+    a.trace = b->trace;
     b->skip_arrive = 0;
     cudaError_t e = decode_launch(b->L, a, pl, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -313,6 +315,12 @@ extern "C" int moe_block_debug_set_wait(moe_block_t* b, uint32_t timeout_us, int
   if (!b) return MOE_ERR_INVALID_ARG;
   b->timeout_ns = timeout_us ? (uint64_t)timeout_us * 1000ull : 500ull * 1000 * 1000;
   b->skip_arrive = skip_arrive ? 1 : 0;
+  return MOE_OK;
+}
+
+extern "C" int moe_block_debug_set_trace(moe_block_t* b, void* trace_device) {
+  if (!b) return MOE_ERR_INVALID_ARG;
+  b->trace = (uint64_t*)trace_device;
   return MOE_OK;
 }
 

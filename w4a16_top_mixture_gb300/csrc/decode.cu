@@ -31,6 +31,28 @@ constexpr int CT = NCW * 32;   // consumer threads
 constexpr int BAR_C = 1;       // named barrier of the consumer warps
 constexpr uint32_t FULL = 0xFFFFFFFFu;
 
+constexpr size_t c_align16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+// Compile-time block shape: every width, stride and loop bound of the decode kernel is a constant, which keeps
+// its machine code small (the kernel's executed code must stay resident in the SM instruction cache).
+template <int H_, int E_, int K_, int I_, int Is_>
+struct Shape {
+  static constexpr int H = H_, E = E_, K = K_, I = I_, Is = Is_;
+  static constexpr int GB = H / 64, GI = I / 64, GS = Is / 64;
+  static constexpr int NCH = H / 32, LW = NCH < 32 ? NCH : 32, P = (NCH + 31) / 32;
+  static constexpr size_t RR = c_align16((size_t)H + (size_t)GB * 4);
+  static constexpr size_t SU = c_align16(2 * (size_t)H + 2 * (size_t)GB * 4);
+  static constexpr size_t SDR = c_align16((size_t)Is + (size_t)GS * 4);
+  static constexpr size_t EU = c_align16((size_t)H + 2 * (size_t)GB * 4);
+  static constexpr size_t DSB = (size_t)H * 4;
+  static constexpr size_t DCB = (size_t)H / 2;
+  static constexpr size_t DB = DSB + 64 * DCB;
+  static constexpr size_t exgu_expert = (size_t)I * EU;
+  static constexpr size_t exdn_expert = (size_t)GI * DB;
+};
+using ShapeProd = Shape<2048, 256, 8, 512, 512>;
+using ShapeTiny = Shape<512, 32, 4, 128, 128>;
+
 struct Ctl {
   uint64_t full[DEC_MAXNS];
   uint64_t empty[DEC_MAXNS];
@@ -49,29 +71,38 @@ struct Ctl {
   uint16_t act_e[512];
   uint32_t act_mask[512];
   int warp_tot[NCW];
+  uint16_t tab_a0[DEC_MAXGRID];   // per CTA: first active-expert index of its unit range
+  uint8_t tab_n[DEC_MAXGRID];     // per CTA: number of segments
 };
 constexpr int CTL_BYTES = (sizeof(Ctl) + 127) & ~127;
 
 struct Smem {   // byte offsets of the dynamic shared-memory regions
-  int xp, xs, hss, hseg, shs, ring;
+  int xh, xs, hss, hseg, shs, ring;
 };
 
-__host__ __device__ inline Smem smem_map(const MoeLayout& L, int T, int grid, int hseg_floats) {
+// xh: x as fp16 [T][P][4 blocks][LW lanes] uint4 (the 8 columns of a block in pair order 0 4 1 5 2 6 3 7);
+// xs: per (token, 32-column chunk) the sums of x over the chunk's "low" and "high" pair columns;
+// hseg: phase B's h, and before phase B the shared expert's hs [T][Is]; hss: 16-column sums of hs;
+// shs: this CTA's shared-down rows; ring: the weight stages.
+template <class LT>
+__host__ __device__ inline Smem smem_map(const LT& L, int T, int grid, int hseg_floats) {
   Smem m;
   int o = CTL_BYTES;
-  m.xp = o;
-  int xbytes = T * L.H * 4, hsbytes = T * L.Is * 4;
-  o += ((xbytes > hsbytes ? xbytes : hsbytes) + 127) & ~127;
-  m.xs = o;   o += (T * L.NCH * 4 + 127) & ~127;
+  m.xh = o;   o += (T * L.H * 2 + 127) & ~127;
+  m.xs = o;   o += (T * L.NCH * 8 + 127) & ~127;
   m.hss = o;  o += (T * (L.Is / 16) * 4 + 127) & ~127;
-  m.hseg = o; o += (hseg_floats * 4 + 127) & ~127;
+  m.hseg = o;
+  {
+    int hx = hseg_floats > T * L.Is ? hseg_floats : T * L.Is;
+    o += (hx * 4 + 127) & ~127;
+  }
   int rpc = (L.H + grid - 1) / grid;
   m.shs = o;  o += (T * rpc * 4 + 127) & ~127;
   m.ring = o;
   return m;
 }
 
-__device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)(((long long)n * c) / G); }
+__device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)(((unsigned)n * (unsigned)c) / (unsigned)G); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -79,132 +110,176 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void stamp(const DecodeArgs& a, int slot) {
+  if (a.trace) a.trace[blockIdx.x * 32 + slot] = globaltimer();
+}
 
 __device__ __forceinline__ void set_error(const DecodeArgs& a, Ctl* ctl, uint32_t bit) {
   atomicOr(a.status, bit);
   ctl->abort = 1;
 }
 
-// Dot products of NR rows (a warp's work item) with TK tokens at a time. Codes: int4 rows in canonical
-// packing (INT8 = false) or permuted int8 rows. Lane l covers the 32-column chunks c = l + LW*p. emit(tc,
-// nt, rs) is called with the warp-reduced row sums rs[tt][r] = sum_c (s_g(c) * dot_c + b_g(c) * xsum_c).
-template <int H, int NR, int TK, bool INT8, typename Emit>
-__device__ __forceinline__ void rows_dot(const uint8_t* const* rowp, const uint8_t* const* sbp, int nvalid,
-                                         const float4* __restrict__ xp, const float* __restrict__ xs,
-                                         const uint8_t* toks, int ntok, Emit emit) {
+template <int NR, int TK>
+struct DotR {
+  float v[TK][NR];
+};
+
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// Dot products of NR rows (a warp's work item) with up to TK tokens. INT8 = false: int4 rows in canonical
+// packing; INT8 = true: permuted int8 rows. Lane l covers the 32-column chunks c = l + LW*p. Every code enters
+// as the exact fp16 value 1024 + q (or 1024 + 16q) and is multiplied by the fp16 activation in an
+// f16 x f16 -> f32 fused multiply-add; the 1024 offsets are removed once per chunk with the chunk's x sums.
+// Returns the warp-reduced sums v[tt][r] = sum_c (s_g(c) * dot_c + b_g(c) * xsum_c) in every lane. Kept out of
+// line: one copy per (NR, INT8) keeps the kernel's executed code within the SM instruction cache.
+template <int H, int NR, int TK, bool INT8>
+__device__ __noinline__ DotR<NR, TK> dot_rows(const uint8_t* r0, const uint8_t* r1, const uint8_t* r2,
+                                              const uint8_t* r3, const uint8_t* s0, const uint8_t* s1,
+                                              const uint8_t* s2, const uint8_t* s3, int nvalid,
+                                              const uint4* __restrict__ xh, const float2* __restrict__ xs, int ta,
+                                              int tb, int nt) {
   constexpr int NCH = H / 32, LW = NCH < 32 ? NCH : 32, P = (NCH + 31) / 32;
   const int lane = threadIdx.x & 31;
-  for (int tc = 0; tc < ntok; tc += TK) {
-    const int nt = min(TK, ntok - tc);
-    int tix[TK];
+  const uint8_t* rp[4] = {r0, r1, r2, r3};
+  const uint8_t* sp[4] = {s0, s1, s2, s3};
+  int tix[TK];
+  tix[0] = ta;
+  if (TK > 1) tix[TK - 1] = tb;
+  DotR<NR, TK> out;
 #pragma unroll
-    for (int tt = 0; tt < TK; ++tt) tix[tt] = tt < nt ? (toks ? (int)toks[tc + tt] : tc + tt) : 0;
-    float rs[TK][NR];
+  for (int tt = 0; tt < TK; ++tt)
 #pragma unroll
-    for (int tt = 0; tt < TK; ++tt)
+    for (int r = 0; r < NR; ++r) out.v[tt][r] = 0.f;
+  if (lane < LW) {
+#pragma unroll 1
+    for (int p = 0; p < P; ++p) {
+      const int c = lane + LW * p;
+      float lo[TK][NR], hi[TK][NR];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) rs[tt][r] = 0.f;
-    if (lane < LW) {
+      for (int tt = 0; tt < TK; ++tt)
 #pragma unroll
-      for (int p = 0; p < P; ++p) {
-        const int c = lane + LW * p;
-        float2 acc[TK][NR];
+        for (int r = 0; r < NR; ++r) lo[tt][r] = hi[tt][r] = 0.f;
+      uint4 ca[NR], cb[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (INT8) {
+          ca[r] = r < nvalid ? *reinterpret_cast<const uint4*>(rp[r] + ((p * 2) * LW + lane) * 16) : make_uint4(0, 0, 0, 0);
+          cb[r] = r < nvalid ? *reinterpret_cast<const uint4*>(rp[r] + ((p * 2 + 1) * LW + lane) * 16) : make_uint4(0, 0, 0, 0);
+        } else {
+          ca[r] = r < nvalid ? *reinterpret_cast<const uint4*>(rp[r] + c * 16) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {   // 8-column block j of the chunk
+        uint4 xv[TK];
 #pragma unroll
         for (int tt = 0; tt < TK; ++tt)
-#pragma unroll
-          for (int r = 0; r < NR; ++r) acc[tt][r] = make_float2(0.f, 0.f);
-        uint4 c4[NR];   // int4: the chunk's 16 bytes (32 codes) of each row
-        if (!INT8) {
-#pragma unroll
-          for (int r = 0; r < NR; ++r)
-            c4[r] = r < nvalid ? *reinterpret_cast<const uint4*>(rowp[r] + c * 16)
-                               : make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {   // int8: one 16-byte load (16 codes) per half chunk
-          uint4 cw[NR];
-#pragma unroll
-          for (int r = 0; r < NR; ++r) {
-            if (INT8)
-              cw[r] = r < nvalid ? *reinterpret_cast<const uint4*>(rowp[r] + ((p * 2 + hh) * LW + lane) * 16)
-                                 : make_uint4(0x80808080u, 0x80808080u, 0x80808080u, 0x80808080u);
-            else
-              cw[r] = c4[r];
-          }
-#pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            const int j = hh * 2 + jj;   // 8-column block within the chunk
-            float4 xa[TK], xb[TK];
-#pragma unroll
-            for (int tt = 0; tt < TK; ++tt) {
-              if (tt < nt) {
-                const int base = ((tix[tt] * P + p) * 8 + j * 2) * LW + lane;
-                xa[tt] = xp[base];
-                xb[tt] = xp[base + LW];
-              } else {
-                xa[tt] = make_float4(0.f, 0.f, 0.f, 0.f);
-                xb[tt] = xa[tt];
-              }
-            }
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-              float2 q[4];
-              if (INT8) {
-                const uint32_t w0 = jj == 0 ? cw[r].x : cw[r].z;
-                const uint32_t w1 = jj == 0 ? cw[r].y : cw[r].w;
-                unpack_int8_pair(w0, w1, q);
-              } else {
-                const uint32_t w = j == 0 ? cw[r].x : j == 1 ? cw[r].y : j == 2 ? cw[r].z : cw[r].w;
-                unpack_int4_word(w, q);
-              }
-#pragma unroll
-              for (int tt = 0; tt < TK; ++tt) {
-                acc[tt][r] = __ffma2_rn(q[0], make_float2(xa[tt].x, xa[tt].y), acc[tt][r]);
-                acc[tt][r] = __ffma2_rn(q[1], make_float2(xa[tt].z, xa[tt].w), acc[tt][r]);
-                acc[tt][r] = __ffma2_rn(q[2], make_float2(xb[tt].x, xb[tt].y), acc[tt][r]);
-                acc[tt][r] = __ffma2_rn(q[3], make_float2(xb[tt].z, xb[tt].w), acc[tt][r]);
-              }
-            }
-          }
-        }
-        // per-chunk affine: s * sum(q x) + b * sum(x)
+          xv[tt] = tt < nt ? xh[((tix[tt] * P + p) * 4 + j) * LW + lane] : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-          if (r < nvalid) {
-            const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(sbp[r] + (c >> 1) * 4));
+          uint32_t v[4];
+          if (INT8) {
+            const uint4& q4 = j < 2 ? ca[r] : cb[r];
+            int8_block_pairs((j & 1) ? q4.z : q4.x, (j & 1) ? q4.w : q4.y, v);
+          } else {
+            int4_word_pairs(j == 0 ? ca[r].x : j == 1 ? ca[r].y : j == 2 ? ca[r].z : ca[r].w, v);
+          }
 #pragma unroll
-            for (int tt = 0; tt < TK; ++tt) {
-              const float X = xs[(tix[tt] * P + p) * LW + lane];
-              rs[tt][r] += sb.x * (acc[tt][r].x + acc[tt][r].y) + sb.y * X;
-            }
+          for (int tt = 0; tt < TK; ++tt) {
+            lo[tt][r] = fmix_lo(v[0], xv[tt].x, lo[tt][r]);
+            lo[tt][r] = fmix_hi(v[0], xv[tt].x, lo[tt][r]);
+            hi[tt][r] = fmix_lo(v[1], xv[tt].y, hi[tt][r]);
+            hi[tt][r] = fmix_hi(v[1], xv[tt].y, hi[tt][r]);
+            lo[tt][r] = fmix_lo(v[2], xv[tt].z, lo[tt][r]);
+            lo[tt][r] = fmix_hi(v[2], xv[tt].z, lo[tt][r]);
+            hi[tt][r] = fmix_lo(v[3], xv[tt].w, hi[tt][r]);
+            hi[tt][r] = fmix_hi(v[3], xv[tt].w, hi[tt][r]);
+          }
+        }
+      }
+      // remove the 1024 offsets, then the group's affine: s * sum(q x) + b * sum(x)
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (r < nvalid) {
+          const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(sp[r] + (c >> 1) * 4));
+#pragma unroll
+          for (int tt = 0; tt < TK; ++tt) {
+            const float2 X = tt < nt ? xs[(tix[tt] * P + p) * LW + lane] : make_float2(0.f, 0.f);
+            const float d = (lo[tt][r] - 1024.0f * X.x) + (hi[tt][r] - 1024.0f * X.y) * (INT8 ? 1.0f : 0.0625f);
+            out.v[tt][r] += sb.x * d + sb.y * (X.x + X.y);
           }
         }
       }
     }
-#pragma unroll
-    for (int tt = 0; tt < TK; ++tt)
-#pragma unroll
-      for (int r = 0; r < NR; ++r) rs[tt][r] = warp_sum(rs[tt][r]);
-    emit(tc, nt, rs);
   }
+#pragma unroll
+  for (int tt = 0; tt < TK; ++tt)
+#pragma unroll
+    for (int r = 0; r < NR; ++r) out.v[tt][r] = warp_sum(out.v[tt][r]);
+  return out;
 }
 
-template <int H, int TK>
-__global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeArgs a, int NS, int SS,
-                                                           int hseg_floats) {
+// Top-k of one token's expert logits held by a warp. Lane l holds experts l*EPL .. l*EPL+EPL-1 (a lower lane
+// means lower indices) as order-preserving integer keys, sorts them descending with a stable odd-even
+// transposition network (equal keys keep ascending indices), then k rounds take the warp maximum of the lane
+// heads, the lowest lane winning ties, and the winning lane pops its head. Lane j < k returns the j-th largest
+// (index, logit).
+template <int EPL>
+__device__ __noinline__ void warp_topk(const float* __restrict__ lg, int E, int K, int lane, int& my_idx,
+                                       float& my_logit) {
+  uint32_t key[EPL];
+  int id[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane * EPL + i;
+    const uint32_t b = e < E ? __float_as_uint(__ldcg(lg + e)) : 0u;
+    key[i] = e < E ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+    id[i] = e;
+  }
+#pragma unroll
+  for (int ph = 0; ph < EPL; ++ph) {
+#pragma unroll
+    for (int i = ph & 1; i + 1 < EPL; i += 2) {
+      const bool sw = key[i] < key[i + 1];
+      const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
+      const int i0 = sw ? id[i + 1] : id[i], i1 = sw ? id[i] : id[i + 1];
+      key[i] = k0; key[i + 1] = k1; id[i] = i0; id[i + 1] = i1;
+    }
+  }
+  my_idx = -1;
+  uint32_t my_key = 0;
+  for (int j = 0; j < K; ++j) {
+    const uint32_t m = __reduce_max_sync(FULL, key[0]);
+    const int win = __ffs(__ballot_sync(FULL, key[0] == m)) - 1;
+    const int sel = __shfl_sync(FULL, id[0], win);
+    if (lane == j) { my_idx = sel; my_key = m; }
+    if (lane == win) {
+#pragma unroll
+      for (int i = 0; i + 1 < EPL; ++i) { key[i] = key[i + 1]; id[i] = id[i + 1]; }
+      key[EPL - 1] = 0u;
+    }
+  }
+  const uint32_t b = (my_key & 0x80000000u) ? (my_key & 0x7FFFFFFFu) : ~my_key;
+  my_logit = __uint_as_float(b);
+}
+
+template <class SH, int TK>
+__global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS, int SS, int hseg_floats) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int NCH = H / 32, LW = NCH < 32 ? NCH : 32, P = (NCH + 31) / 32;
+  constexpr SH L{};
+  constexpr int H = SH::H, NCH = SH::NCH, LW = SH::LW, P = SH::P;
+  constexpr int E = SH::E, K = SH::K, I = SH::I, Is = SH::Is;
   const int G = gridDim.x, cta = blockIdx.x;
-  const int T = a.T, E = L.E, K = L.K, I = L.I, Is = L.Is;
+  const int T = a.T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
   const Smem sm = smem_map(L, T, G, hseg_floats);
-  float4* xp = reinterpret_cast<float4*>(smem + sm.xp);
-  float* xs = reinterpret_cast<float*>(smem + sm.xs);
-  float* hsp = reinterpret_cast<float*>(smem + sm.xp);   // shared-expert h (aliases x after phase B)
+  uint4* xh = reinterpret_cast<uint4*>(smem + sm.xh);
+  float2* xs = reinterpret_cast<float2*>(smem + sm.xs);
   float* hss = reinterpret_cast<float*>(smem + sm.hss);
   float* hseg = reinterpret_cast<float*>(smem + sm.hseg);
+  float* hsn = hseg;   // shared-expert hs [T][Is], natural order, used before phase B
   float* shs = reinterpret_cast<float*>(smem + sm.shs);
   uint8_t* ring = smem + sm.ring;
 
@@ -219,6 +294,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
   const int SDPI = SS / (int)L.SDR;               // shared-down rows per item
 
   if (threadIdx.x == 0) {
+#pragma unroll 1
     for (int s = 0; s < NS; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], NCW);
@@ -229,207 +305,237 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
     fence_mbar_init();
   }
   __syncthreads();
+  if (threadIdx.x == 0) stamp(a, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      int n = 0;
+      int n = 0, ps = 0;      // items issued, ring stage of the next one
+      uint32_t pph = 0;       // wrap parity of the ring
       const uint64_t pol = policy_evict_first();
       auto issue = [&](const uint8_t* src, uint32_t bytes) -> bool {
         if (ctl->abort) return false;
-        const int s = n % NS;
-        if (n >= NS && !mbar_wait(&ctl->empty[s], ((n / NS) - 1) & 1, a.timeout_ns)) {
+        if (n >= NS && !mbar_wait(&ctl->empty[ps], pph ^ 1u, a.timeout_ns)) {
           set_error(a, ctl, ERR_WAIT_EMPTY);
           return false;
         }
-        mbar_expect_tx(&ctl->full[s], bytes);
-        bulk_g2s_hint(ring + (size_t)s * SS, src, bytes, &ctl->full[s], pol);
+        mbar_expect_tx(&ctl->full[ps], bytes);
+        bulk_g2s_hint(ring + (size_t)ps * SS, src, bytes, &ctl->full[ps], pol);
         ++n;
+        if (++ps == NS) { ps = 0; pph ^= 1u; }
         return true;
       };
       bool ok = true;
-      for (int r = ra; ok && r < rb; r += RPI) {
-        const int nr = min(RPI, rb - r);
-        ok = issue(a.router + (size_t)r * L.RR, (uint32_t)(nr * L.RR));
-      }
-      for (int u = sa; ok && u < sbn; u += SPI) {
-        const int nu = min(SPI, sbn - u);
-        ok = issue(a.sh_gu + (size_t)u * L.SU, (uint32_t)(nu * L.SU));
-      }
+#pragma unroll 1
+      for (int r = ra; ok && r < rb; r += RPI)
+        ok = issue(a.router + (size_t)r * L.RR, (uint32_t)(min(RPI, rb - r) * L.RR));
+#pragma unroll 1
+      for (int u = sa; ok && u < sbn; u += SPI)
+        ok = issue(a.sh_gu + (size_t)u * L.SU, (uint32_t)(min(SPI, sbn - u) * L.SU));
+#pragma unroll 1
+      for (int r = r0; ok && r < r1; r += SDPI)
+        ok = issue(a.sh_dn + (size_t)r * L.SDR, (uint32_t)(min(SDPI, r1 - r) * L.SDR));
+      stamp(a, 16);
       if (ok && !mbar_wait(&ctl->route_ready, 0, a.timeout_ns * 4)) {
         set_error(a, ctl, ERR_WAIT_ROUTE);
         ok = false;
       }
       if (ok && ctl->abort) ok = false;
+      stamp(a, 17);
       const int nseg = ok ? ctl->nseg : 0;
+#pragma unroll 1
       for (int sgi = 0; ok && sgi < nseg; ++sgi) {
         const int e = ctl->seg_e[sgi], u0 = ctl->seg_u0[sgi], u1 = ctl->seg_u1[sgi];
         const uint8_t* gu = a.ex_gu + (size_t)e * L.exgu_expert;
+#pragma unroll 1
         for (int u = u0; ok && u < u1; u += UPI)
           ok = issue(gu + (size_t)u * L.EU, (uint32_t)(min(UPI, u1 - u) * L.EU));
         const uint8_t* dn = a.ex_dn + (size_t)e * L.exdn_expert;
+#pragma unroll 1
         for (int g = u0 / 64; ok && g * 64 < u1; ++g) {
           const uint8_t* blk = dn + (size_t)g * L.DB;
           ok = issue(blk, (uint32_t)L.DSB);
           const int ga = max(u0, g * 64), gb = min(u1, g * 64 + 64);
+#pragma unroll 1
           for (int u = ga; ok && u < gb; u += DPI)
             ok = issue(blk + L.DSB + (size_t)(u - g * 64) * L.DCB, (uint32_t)(min(DPI, gb - u) * L.DCB));
         }
       }
-      for (int r = r0; ok && r < r1; r += SDPI)
-        ok = issue(a.sh_dn + (size_t)r * L.SDR, (uint32_t)(min(SDPI, r1 - r) * L.SDR));
+      stamp(a, 18);
       // drain: every issued copy must have landed before the CTA may leave
-      for (int m = max(0, n - NS); m < n; ++m)
-        if (!mbar_wait(&ctl->full[m % NS], (m / NS) & 1, a.timeout_ns)) atomicOr(a.status, ERR_WAIT_FULL);
+      {
+        // the last min(n, NS) issued items, oldest first: walk back from the next stage
+        const int cnt = min(n, NS);
+        int s = ps - cnt;
+        uint32_t ph = pph;
+        if (s < 0) { s += NS; ph ^= 1u; }
+#pragma unroll 1
+        for (int m = 0; m < cnt; ++m) {
+          if (!mbar_wait(&ctl->full[s], ph, a.timeout_ns)) atomicOr(a.status, ERR_WAIT_FULL);
+          if (++s == NS) { s = 0; ph ^= 1u; }
+        }
+      }
+      stamp(a, 19);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ consumers
     const int cw = warp - 1;
     const int ctid = threadIdx.x - 32;
-    int it = 0;   // item counter, mirrors the producer's
+    int cs = 0;            // ring stage of the next item, mirrors the producer's order
+    uint32_t cph = 0;      // its phase parity
     auto acquire = [&]() -> const uint8_t* {
-      const int s = it % NS;
-      if (!ctl->abort && !mbar_wait(&ctl->full[s], (it / NS) & 1, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_FULL);
-      return ring + (size_t)s * SS;
+      if (!ctl->abort && !mbar_wait(&ctl->full[cs], cph, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_FULL);
+      return ring + (size_t)cs * SS;
     };
     auto release = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->empty[it % NS]);
-      ++it;
+      if (lane == 0) mbar_arrive(&ctl->empty[cs]);
+      if (++cs == NS) { cs = 0; cph ^= 1u; }
     };
 
-    // ---- x prologue: (RMSNorm) -> fp16 -> fp32, permuted for the row dots, plus 32-column sums
+    // ---- x prologue: (RMSNorm ->) fp16 activations in pair order, plus per-chunk pair-column sums
     for (int t = cw; t < T; t += NCW) {
       const uint16_t* xr = a.x + (size_t)t * H;
-      float v[P][32];
-      float ss = 0.f;
-#pragma unroll
-      for (int p = 0; p < P; ++p) {
-        const int c = lane + LW * p;
-        if (lane < LW) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 raw = *reinterpret_cast<const uint4*>(xr + c * 32 + q4 * 8);
-            const __half2* hv = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float2 f = __half22float2(hv[k]);
-              v[p][q4 * 8 + 2 * k] = f.x;
-              v[p][q4 * 8 + 2 * k + 1] = f.y;
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 32; ++k) ss += v[p][k] * v[p][k];
-        }
-      }
+      float rn = 1.f;
       if (a.gamma) {
-        ss = warp_sum(ss);
-        const float rn = 1.0f / sqrtf(ss / (float)H + a.eps);
+        float ss = 0.f;
+#pragma unroll 1
+        for (int i = lane * 8; i < H; i += 256) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(xr + i);
+          const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(hv[k]);
+            ss += f.x * f.x + f.y * f.y;
+          }
+        }
+        ss = warp_sum(ss);
+        rn = 1.0f / sqrtf(ss / (float)H + a.eps);
+      }
+      if (lane < LW) {
+#pragma unroll 1
         for (int p = 0; p < P; ++p) {
           const int c = lane + LW * p;
-          if (lane < LW) {
+          uint4 raw[4];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const float g = __half2float(__ushort_as_half(a.gamma[c * 32 + k]));
-              v[p][k] = __half2float(__float2half_rn(v[p][k] * rn * g));
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int p = 0; p < P; ++p) {
-        if (lane < LW) {
-          float sum = 0.f;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) sum += v[p][k];
-          xs[(t * P + p) * LW + lane] = sum;
+          for (int j = 0; j < 4; ++j) raw[j] = *reinterpret_cast<const uint4*>(xr + c * 32 + j * 8);
+          float xl = 0.f, xhs = 0.f;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float* b8 = &v[p][8 * j];
-            const int base = ((t * P + p) * 8 + j * 2) * LW + lane;
-            xp[base] = make_float4(b8[0], b8[4], b8[1], b8[5]);
-            xp[base + LW] = make_float4(b8[2], b8[6], b8[3], b8[7]);
+            __half h8[8];
+            *reinterpret_cast<uint4*>(h8) = raw[j];
+            if (a.gamma) {
+              const uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + c * 32 + j * 8);
+              const __half* g8 = reinterpret_cast<const __half*>(&graw);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                h8[k] = __float2half_rn(__half2float(h8[k]) * rn * __half2float(g8[k]));
+            }
+            // pair order (0,4) (1,5) (2,6) (3,7); "low" columns 0 4 2 6, "high" columns 1 5 3 7
+            uint4 o;
+            o.x = (uint32_t)__half_as_ushort(h8[0]) | ((uint32_t)__half_as_ushort(h8[4]) << 16);
+            o.y = (uint32_t)__half_as_ushort(h8[1]) | ((uint32_t)__half_as_ushort(h8[5]) << 16);
+            o.z = (uint32_t)__half_as_ushort(h8[2]) | ((uint32_t)__half_as_ushort(h8[6]) << 16);
+            o.w = (uint32_t)__half_as_ushort(h8[3]) | ((uint32_t)__half_as_ushort(h8[7]) << 16);
+            xh[((t * P + p) * 4 + j) * LW + lane] = o;
+            xl += (__half2float(h8[0]) + __half2float(h8[4])) + (__half2float(h8[2]) + __half2float(h8[6]));
+            xhs += (__half2float(h8[1]) + __half2float(h8[5])) + (__half2float(h8[3]) + __half2float(h8[7]));
           }
+          xs[(t * P + p) * LW + lane] = make_float2(xl, xhs);
         }
       }
     }
     named_bar(BAR_C, CT);
+    if (ctid == 0) stamp(a, 1);
 
-    // ---- A1: router rows
+    // ---- A1: router rows -> logits (a row per warp)
     for (int r = ra; r < rb; r += RPI) {
       const int nr = min(RPI, rb - r);
       const uint8_t* st = acquire();
       if (!ctl->abort) {
         for (int rr = cw; rr < nr; rr += NCW) {
-          const uint8_t* rowp[1] = {st + (size_t)rr * L.RR};
-          const uint8_t* sbp[1] = {st + (size_t)rr * L.RR + H};
-          const int row = r + rr;
-          rows_dot<H, 1, TK, true>(rowp, sbp, 1, xp, xs, nullptr, T, [&](int tc, int nt, float (*rs)[1]) {
+          const uint8_t* b0 = st + (size_t)rr * L.RR;
+          for (int tc = 0; tc < T; tc += TK) {
+            const int nt = min(TK, T - tc);
+            const DotR<1, TK> d = dot_rows<H, 1, TK, true>(b0, b0, b0, b0, b0 + H, b0 + H, b0 + H, b0 + H, 1, xh, xs,
+                                                           tc, tc + TK - 1, nt);
             if (lane == 0)
-              for (int tt = 0; tt < nt; ++tt) a.logits[(size_t)(tc + tt) * (E + 1) + row] = rs[tt][0];
-          });
+#pragma unroll
+              for (int tt = 0; tt < TK; ++tt)
+                if (tt < nt) a.logits[(size_t)(tc + tt) * (E + 1) + r + rr] = d.v[tt][0];
+          }
         }
       }
       release();
     }
     named_bar(BAR_C, CT);
-    if (ctid == 0 && !(a.skip_arrive && cta == 0)) {
+    if (ctid == 0) {
+      stamp(a, 2);
+      if (!(a.skip_arrive && cta == 0)) {
+        __threadfence();
+        atomicAdd(&a.counters[0], 1u);
+      }
+    }
+
+    // ---- A2: shared-expert gate/up units, a pair per warp (overlaps the wait for every CTA's logits)
+#pragma unroll 1
+    for (int u = sa; u < sbn; u += SPI) {
+      const int nu = min(SPI, sbn - u);
+      const uint8_t* st = acquire();
+      if (!ctl->abort) {
+#pragma unroll 1
+        for (int pr = cw; pr * 2 < nu; pr += NCW) {
+          const uint8_t* ub = st + (size_t)(2 * pr) * L.SU;
+          const int nvalid = (2 * pr + 1 < nu) ? 4 : 2;
+          const int i0 = u + 2 * pr;
+#pragma unroll 1
+          for (int tc = 0; tc < T; tc += TK) {
+            const int nt = min(TK, T - tc);
+            const DotR<4, TK> d = dot_rows<H, 4, TK, true>(ub, ub + H, ub + L.SU, ub + L.SU + H, ub + 2 * H,
+                                                           ub + 2 * H + L.GB * 4, ub + L.SU + 2 * H,
+                                                           ub + L.SU + 2 * H + L.GB * 4, nvalid, xh, xs, tc, tc + TK - 1,
+                                                           nt);
+            if (lane < 2 * TK) {
+              const int tt = lane >> 1, k = lane & 1;
+              float g = 0.f, up = 0.f;
+#pragma unroll
+              for (int q = 0; q < TK; ++q)
+                if (q == tt) { g = k ? d.v[q][2] : d.v[q][0]; up = k ? d.v[q][3] : d.v[q][1]; }
+              if (tt < nt && 2 * k < nvalid) a.hs[(size_t)(tc + tt) * Is + i0 + k] = silu_fast(g) * up;
+            }
+          }
+        }
+      }
+      release();
+    }
+    named_bar(BAR_C, CT);
+    if (ctid == 0) {
       __threadfence();
-      atomicAdd(&a.counters[0], 1u);
+      atomicAdd(&a.counters[1], 1u);
+      stamp(a, 6);
     }
 
     // ---- R: routing (every CTA, every token)
     if (ctid == 0 && !ctl->abort && !spin_geq(&a.counters[0], (uint32_t)G, a.timeout_ns))
       set_error(a, ctl, ERR_WAIT_LOGITS);
+    if (ctid == 0) stamp(a, 3);
     named_bar(BAR_C, CT);
-    __threadfence();
     if (!ctl->abort) {
-      const int EPL = (E + 31) / 32;
+#pragma unroll 1
       for (int t = cw; t < T; t += NCW) {
         const float* lg = a.logits + (size_t)t * (E + 1);
-        uint32_t key[16];
-        float val[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = lane * EPL + i;
-          const bool in = i < EPL && e < E;
-          const float v = in ? __ldcg(lg + e) : 0.f;
-          const uint32_t b = __float_as_uint(v);
-          key[i] = in ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
-          val[i] = v;
-        }
-        int my_idx = -1;
-        float my_logit = 0.f;
-        for (int j = 0; j < K; ++j) {
-          uint32_t best = 0;
-          int bi = 0;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (key[i] > best) { best = key[i]; bi = i; }
-          const uint32_t m = __reduce_max_sync(FULL, best);
-          const int win = __ffs(__ballot_sync(FULL, best == m)) - 1;
-          float lv = 0.f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (i == bi) lv = val[i];
-          if (lane == win) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (i == bi) key[i] = 0u;
-          }
-          const int sel = __shfl_sync(FULL, lane * EPL + bi, win);
-          const float sl = __shfl_sync(FULL, lv, win);
-          if (lane == j) { my_idx = sel; my_logit = sl; }
-        }
+        int my_idx;
+        float my_logit;
+        warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit);
         const float mx = __shfl_sync(FULL, my_logit, 0);
         const float ex = lane < K ? expf(my_logit - mx) : 0.f;
         const float Z = warp_sum(ex);
         int rank = 0;
+#pragma unroll 1
         for (int i = 0; i < K; ++i) {
           const int oi = __shfl_sync(FULL, my_idx, i);
-          rank += (lane < K && oi < my_idx) ? 1 : 0;
+          rank += (oi < my_idx) ? 1 : 0;
         }
         if (lane < K) {
           ctl->ids[t][rank] = my_idx;
@@ -442,18 +548,28 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
       }
     }
     named_bar(BAR_C, CT);
+    if (ctid == 0) stamp(a, 4);
     // bucketing: token masks per expert, active experts in ascending order
-    for (int e = ctid; e < E; e += CT) ctl->emask[e] = 0u;
-    named_bar(BAR_C, CT);
-    if (!ctl->abort)
-      for (int p = ctid; p < T * K; p += CT) atomicOr(&ctl->emask[ctl->ids[p / K][p % K]], 1u << (p / K));
-    named_bar(BAR_C, CT);
-    {
+    if (T == 1) {
+      if (ctid < K) {
+        ctl->act_e[ctid] = (uint16_t)ctl->ids[0][ctid];
+        ctl->act_mask[ctid] = 1u;
+      }
+      if (ctid == 0) ctl->U = ctl->abort ? 0 : K;
+    } else {
+#pragma unroll 1
+      for (int e = ctid; e < E; e += CT) ctl->emask[e] = 0u;
+      named_bar(BAR_C, CT);
+      if (!ctl->abort)
+#pragma unroll 1
+        for (int p = ctid; p < T * K; p += CT) atomicOr(&ctl->emask[ctl->ids[p / K][p % K]], 1u << (p / K));
+      named_bar(BAR_C, CT);
       const uint32_t msk = ctid < E ? ctl->emask[ctid] : 0u;
       const uint32_t bal = __ballot_sync(FULL, msk != 0u);
       if (lane == 0) ctl->warp_tot[cw] = __popc(bal);
       named_bar(BAR_C, CT);
       int base = 0;
+#pragma unroll 1
       for (int w = 0; w < cw; ++w) base += ctl->warp_tot[w];
       if (msk != 0u) {
         const int pos = base + __popc(bal & ((1u << lane) - 1u));
@@ -463,112 +579,183 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
       if (ctid == CT - 1) ctl->U = base + __popc(bal);
     }
     named_bar(BAR_C, CT);
-    if (ctid == 0) {
+    {
       const int U = ctl->U;
       const int N = U * I;
-      const int lo = range_lo(N, cta, G), hi = range_lo(N, cta + 1, G);
-      int nseg = 0;
-      for (int aa = lo / I; aa * I < hi && lo < hi; ++aa) {
-        if (nseg == DEC_MAXSEG) { set_error(a, ctl, ERR_SEGMENTS); break; }
-        const int e = ctl->act_e[aa];
-        const uint32_t msk = ctl->act_mask[aa];
-        ctl->seg_a[nseg] = aa;
-        ctl->seg_e[nseg] = e;
-        ctl->seg_u0[nseg] = max(lo, aa * I) - aa * I;
-        ctl->seg_u1[nseg] = min(hi, (aa + 1) * I) - aa * I;
-        int n = 0;
-        for (int t = 0; t < T; ++t) {
-          if (msk & (1u << t)) {
-            ctl->seg_tok[nseg][n] = (uint8_t)t;
-            float wv = 0.f;
-            for (int j = 0; j < K; ++j)
-              if (ctl->ids[t][j] == e) wv = ctl->wts[t][j];
-            ctl->seg_w[nseg][n] = wv;
-            ++n;
+      // segment table of every CTA (for the final reduction)
+#pragma unroll 1
+      for (int c = ctid; c < G; c += CT) {
+        const int lo = range_lo(N, c, G), hi = range_lo(N, c + 1, G);
+        ctl->tab_a0[c] = (uint16_t)(lo / I);
+        ctl->tab_n[c] = (uint8_t)(lo < hi ? (hi - 1) / I - lo / I + 1 : 0);
+      }
+      if (ctid == 0) {
+        const int lo = range_lo(N, cta, G), hi = range_lo(N, cta + 1, G);
+        int nseg = 0;
+#pragma unroll 1
+        for (int aa = lo / I; aa * I < hi && lo < hi; ++aa) {
+          if (nseg == DEC_MAXSEG) { set_error(a, ctl, ERR_SEGMENTS); break; }
+          const int e = ctl->act_e[aa];
+          const uint32_t msk = ctl->act_mask[aa];
+          ctl->seg_e[nseg] = e;
+          ctl->seg_u0[nseg] = max(lo, aa * I) - aa * I;
+          ctl->seg_u1[nseg] = min(hi, (aa + 1) * I) - aa * I;
+          int n = 0;
+#pragma unroll 1
+          for (int t = 0; t < T; ++t) {
+            if (msk & (1u << t)) {
+              ctl->seg_tok[nseg][n] = (uint8_t)t;
+              float wv = 0.f;
+#pragma unroll 1
+              for (int j = 0; j < K; ++j)
+                if (ctl->ids[t][j] == e) wv = ctl->wts[t][j];
+              ctl->seg_w[nseg][n] = wv;
+              ++n;
+            }
+          }
+          ctl->seg_n[nseg] = n;
+          const int units = ctl->seg_u1[nseg] - ctl->seg_u0[nseg];
+          if (units * n > hseg_floats) set_error(a, ctl, ERR_HSEG);
+          ++nseg;
+        }
+        ctl->nseg = ctl->abort ? 0 : nseg;
+        mbar_arrive(&ctl->route_ready);
+        stamp(a, 5);
+        if (cta == 0 && a.rec_ids) {
+#pragma unroll 1
+          for (int t = 0; t < T; ++t) {
+#pragma unroll 1
+            for (int j = 0; j < K; ++j) {
+              a.rec_ids[t * K + j] = ctl->ids[t][j];
+              a.rec_w[t * K + j] = ctl->wts[t][j];
+            }
+            a.rec_sg[t] = ctl->sg[t];
           }
         }
-        ctl->seg_n[nseg] = n;
-        const int units = ctl->seg_u1[nseg] - ctl->seg_u0[nseg];
-        if (units * n > hseg_floats) set_error(a, ctl, ERR_HSEG);
-        ++nseg;
       }
-      ctl->nseg = ctl->abort ? 0 : nseg;
-      if (cta == 0 && a.rec_ids) {
-        for (int t = 0; t < T; ++t) {
-          for (int j = 0; j < K; ++j) {
-            a.rec_ids[t * K + j] = ctl->ids[t][j];
-            a.rec_w[t * K + j] = ctl->wts[t][j];
-          }
-          a.rec_sg[t] = ctl->sg[t];
-        }
-      }
-      mbar_arrive(&ctl->route_ready);
     }
     named_bar(BAR_C, CT);
 
-    // ---- A2: shared-expert gate/up units (pairs of units per warp)
-    for (int u = sa; u < sbn; u += SPI) {
-      const int nu = min(SPI, sbn - u);
+    // ---- C: shared down rows (every CTA's hs; the routed weights are in flight meanwhile)
+    if (ctid == 0 && !ctl->abort && !spin_geq(&a.counters[1], (uint32_t)G, a.timeout_ns))
+      set_error(a, ctl, ERR_WAIT_HS);
+    named_bar(BAR_C, CT);
+    if (!ctl->abort)
+#pragma unroll 1
+      for (int i = ctid; i < T * Is / 4; i += CT)
+        reinterpret_cast<float4*>(hsn)[i] = __ldcg(reinterpret_cast<const float4*>(a.hs) + i);
+    named_bar(BAR_C, CT);
+    if (!ctl->abort)
+#pragma unroll 1
+      for (int i = ctid; i < T * (Is / 16); i += CT) {
+        const float4* src = reinterpret_cast<const float4*>(hsn + (size_t)i * 16);
+        const float4 p0 = src[0], p1 = src[1], p2 = src[2], p3 = src[3];
+        hss[i] = ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w)) +
+                 ((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w));
+      }
+    named_bar(BAR_C, CT);
+    if (ctid == 0) stamp(a, 9);
+#pragma unroll 1
+    for (int r = r0; r < r1; r += SDPI) {
+      const int nr = min(SDPI, r1 - r);
       const uint8_t* st = acquire();
       if (!ctl->abort) {
-        for (int pr = cw; pr * 2 < nu; pr += NCW) {
-          const uint8_t* ub = st + (size_t)(2 * pr) * L.SU;
-          const uint8_t* rowp[4] = {ub, ub + H, ub + L.SU, ub + L.SU + H};
-          const uint8_t* sbp[4] = {ub + 2 * H, ub + 2 * H + L.GB * 4, ub + L.SU + 2 * H,
-                                   ub + L.SU + 2 * H + L.GB * 4};
-          const int nvalid = (2 * pr + 1 < nu) ? 4 : 2;
-          const int i0 = u + 2 * pr;
-          rows_dot<H, 4, TK, true>(rowp, sbp, nvalid, xp, xs, nullptr, T, [&](int tc, int nt, float (*rs)[4]) {
-            if (lane == 0)
-              for (int tt = 0; tt < nt; ++tt) {
-                a.hs[(size_t)(tc + tt) * Is + i0] = silu_f(rs[tt][0]) * rs[tt][1];
-                if (nvalid == 4) a.hs[(size_t)(tc + tt) * Is + i0 + 1] = silu_f(rs[tt][2]) * rs[tt][3];
+#pragma unroll 1
+        for (int rr = cw; rr < nr; rr += NCW) {
+          const uint8_t* row = st + (size_t)rr * L.SDR;
+#pragma unroll 1
+          for (int tc = 0; tc < T; tc += TK) {
+            const int nt = min(TK, T - tc);
+            float rs[TK];
+#pragma unroll
+            for (int tt = 0; tt < TK; ++tt) rs[tt] = 0.f;
+#pragma unroll 1
+            for (int cc = lane; cc < Is / 16; cc += 32) {
+              const uint4 cw4 = *reinterpret_cast<const uint4*>(row + cc * 16);
+              const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + Is + (cc >> 2) * 4));
+              float2 q[8];
+              unpack_int8_word(cw4.x, q[0], q[1]);
+              unpack_int8_word(cw4.y, q[2], q[3]);
+              unpack_int8_word(cw4.z, q[4], q[5]);
+              unpack_int8_word(cw4.w, q[6], q[7]);
+#pragma unroll
+              for (int tt = 0; tt < TK; ++tt) {
+                if (tt < nt) {
+                  const float4* hv = reinterpret_cast<const float4*>(hsn + (size_t)(tc + tt) * Is + cc * 16);
+                  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                  for (int m = 0; m < 4; ++m) {
+                    const float4 h4 = hv[m];
+                    acc = __ffma2_rn(q[2 * m], make_float2(h4.x, h4.y), acc);
+                    acc = __ffma2_rn(q[2 * m + 1], make_float2(h4.z, h4.w), acc);
+                  }
+                  rs[tt] += sb.x * (acc.x + acc.y) + sb.y * hss[(tc + tt) * (Is / 16) + cc];
+                }
               }
-          });
+            }
+#pragma unroll
+            for (int tt = 0; tt < TK; ++tt) rs[tt] = warp_sum(rs[tt]);
+            if (lane == 0)
+#pragma unroll 1
+              for (int tt = 0; tt < nt; ++tt) shs[(tc + tt) * (r1 - r0) + (r + rr - r0)] = rs[tt];
+          }
         }
       }
       release();
     }
     named_bar(BAR_C, CT);
-    if (ctid == 0) {
-      __threadfence();
-      atomicAdd(&a.counters[1], 1u);
-    }
+    if (ctid == 0) stamp(a, 10);
 
     // ---- B: routed segments
     const int nseg = ctl->nseg;
+#pragma unroll 1
     for (int sgi = 0; sgi < nseg; ++sgi) {
       const int u0 = ctl->seg_u0[sgi], u1 = ctl->seg_u1[sgi], ne = ctl->seg_n[sgi];
       const int units = u1 - u0;
       const uint8_t* toks = ctl->seg_tok[sgi];
-      // gate/up -> h
+      // gate/up -> h, a pair of units per warp
+#pragma unroll 1
       for (int u = u0; u < u1; u += UPI) {
         const int nu = min(UPI, u1 - u);
         const uint8_t* st = acquire();
         if (!ctl->abort) {
+#pragma unroll 1
           for (int pr = cw; pr * 2 < nu; pr += NCW) {
             const uint8_t* ub = st + (size_t)(2 * pr) * L.EU;
-            const uint8_t* rowp[4] = {ub, ub + H / 2, ub + L.EU, ub + L.EU + H / 2};
-            const uint8_t* sbp[4] = {ub + H, ub + H + L.GB * 4, ub + L.EU + H, ub + L.EU + H + L.GB * 4};
             const int nvalid = (2 * pr + 1 < nu) ? 4 : 2;
             const int ul = u + 2 * pr - u0;
-            rows_dot<H, 4, TK, false>(rowp, sbp, nvalid, xp, xs, toks, ne, [&](int tc, int nt, float (*rs)[4]) {
-              if (lane == 0)
-                for (int tt = 0; tt < nt; ++tt) {
-                  hseg[(tc + tt) * units + ul] = silu_f(rs[tt][0]) * rs[tt][1];
-                  if (nvalid == 4) hseg[(tc + tt) * units + ul + 1] = silu_f(rs[tt][2]) * rs[tt][3];
-                }
-            });
+#pragma unroll 1
+            for (int tc = 0; tc < ne; tc += TK) {
+              const int nt = min(TK, ne - tc);
+              const DotR<4, TK> d = dot_rows<H, 4, TK, false>(ub, ub + H / 2, ub + L.EU, ub + L.EU + H / 2,
+                                                              ub + H, ub + H + L.GB * 4, ub + L.EU + H,
+                                                              ub + L.EU + H + L.GB * 4, nvalid, xh, xs, toks[tc],
+                                                              toks[tc + nt - 1], nt);
+              if (lane < 2 * TK) {
+                const int tt = lane >> 1, k = lane & 1;
+                float g = 0.f, up = 0.f;
+#pragma unroll
+                for (int q = 0; q < TK; ++q)
+                  if (q == tt) { g = k ? d.v[q][2] : d.v[q][0]; up = k ? d.v[q][3] : d.v[q][1]; }
+                if (tt < nt && 2 * k < nvalid) hseg[(tc + tt) * units + ul + k] = silu_fast(g) * up;
+              }
+            }
           }
         }
         release();
       }
       named_bar(BAR_C, CT);
-      // down: per group, the (s,b) block then the unit columns
-      const int hq = ctid;   // row quad
+      if (ctid == 0 && sgi == 0) stamp(a, 7);
+      // down: per group, the (s,b) block then the unit columns; each thread owns 4 output rows
+      const int hq = ctid;
       const bool has_q = hq < H / 4;
+      const bool in_regs = ne <= TK;   // all tokens' partial sums stay in registers across the segment
+      float4 pacc[TK];
+#pragma unroll
+      for (int tt = 0; tt < TK; ++tt) pacc[tt] = make_float4(0.f, 0.f, 0.f, 0.f);
       bool first = true;
       const size_t slot0 = ((size_t)cta * DEC_MAXSEG + sgi) * T;
+#pragma unroll 1
       for (int g = u0 / 64; g * 64 < u1; ++g) {
         float2 sbq[4];
         {
@@ -580,10 +767,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
           release();
         }
         const int ga = max(u0, g * 64), gb = min(u1, g * 64 + 64);
+#pragma unroll 1
         for (int u = ga; u < gb; u += DPI) {
           const int nu = min(DPI, gb - u);
           const uint8_t* st = acquire();
           if (!ctl->abort && has_q) {
+#pragma unroll 1
             for (int tc = 0; tc < ne; tc += TK) {
               const int nt = min(TK, ne - tc);
               float2 acc[TK][2];
@@ -593,15 +782,16 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
                 acc[tt][0] = acc[tt][1] = make_float2(0.f, 0.f);
                 hsum[tt] = 0.f;
               }
+              const float* hrow = hseg + (size_t)tc * units + (u - u0);
+#pragma unroll 2
               for (int k = 0; k < nu; ++k) {
                 const uint32_t hw = *reinterpret_cast<const uint16_t*>(st + (size_t)k * L.DCB + hq * 2);
                 float2 q01, q23;
                 unpack_int4_quad(hw, q01, q23);
-                const int ul = u + k - u0;
 #pragma unroll
                 for (int tt = 0; tt < TK; ++tt) {
                   if (tt < nt) {
-                    const float h = hseg[(tc + tt) * units + ul];
+                    const float h = hrow[tt * units + k];
                     acc[tt][0] = __ffma2_rn(q01, make_float2(h, h), acc[tt][0]);
                     acc[tt][1] = __ffma2_rn(q23, make_float2(h, h), acc[tt][1]);
                     hsum[tt] += h;
@@ -617,12 +807,16 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
                   v.y = w * (sbq[1].x * acc[tt][0].y + sbq[1].y * hsum[tt]);
                   v.z = w * (sbq[2].x * acc[tt][1].x + sbq[2].y * hsum[tt]);
                   v.w = w * (sbq[3].x * acc[tt][1].y + sbq[3].y * hsum[tt]);
-                  float4* dst = reinterpret_cast<float4*>(a.partial + (slot0 + tc + tt) * H + 4 * hq);
-                  if (!first) {
-                    const float4 o = __ldcg(dst);
-                    v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                  if (in_regs) {
+                    pacc[tt].x += v.x; pacc[tt].y += v.y; pacc[tt].z += v.z; pacc[tt].w += v.w;
+                  } else {
+                    float4* dst = reinterpret_cast<float4*>(a.partial + (slot0 + tc + tt) * H + 4 * hq);
+                    if (!first) {
+                      const float4 o = __ldcg(dst);
+                      v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                    }
+                    __stcg(dst, v);
                   }
-                  __stcg(dst, v);
                 }
               }
             }
@@ -631,104 +825,44 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
           release();
         }
       }
+      if (in_regs && !ctl->abort && has_q) {
+#pragma unroll
+        for (int tt = 0; tt < TK; ++tt)
+          if (tt < ne) __stcg(reinterpret_cast<float4*>(a.partial + (slot0 + tt) * H + 4 * hq), pacc[tt]);
+      }
       named_bar(BAR_C, CT);
     }
-
-    // ---- C: shared down rows (needs every CTA's hs)
-    if (ctid == 0 && !ctl->abort && !spin_geq(&a.counters[1], (uint32_t)G, a.timeout_ns))
-      set_error(a, ctl, ERR_WAIT_HS);
-    named_bar(BAR_C, CT);
-    __threadfence();
-    if (!ctl->abort) {
-      // stage hs permuted in 8-blocks (0,4,1,5,2,6,3,7) and its 16-column sums
-      for (int i = ctid; i < T * Is / 8; i += CT) {
-        const int t = i / (Is / 8), blk = i % (Is / 8);
-        const float4 lo = __ldcg(reinterpret_cast<const float4*>(a.hs + (size_t)t * Is + blk * 8));
-        const float4 hi = __ldcg(reinterpret_cast<const float4*>(a.hs + (size_t)t * Is + blk * 8 + 4));
-        float4* d = reinterpret_cast<float4*>(hsp + (size_t)t * Is + blk * 8);
-        d[0] = make_float4(lo.x, hi.x, lo.y, hi.y);
-        d[1] = make_float4(lo.z, hi.z, lo.w, hi.w);
-      }
-      for (int i = ctid; i < T * (Is / 16); i += CT) {
-        const int t = i / (Is / 16), c = i % (Is / 16);
-        const float* src = a.hs + (size_t)t * Is + c * 16;
-        float s = 0.f;
-        for (int k = 0; k < 16; ++k) s += __ldcg(src + k);
-        hss[i] = s;
-      }
-    }
-    named_bar(BAR_C, CT);
-    for (int r = r0; r < r1; r += SDPI) {
-      const int nr = min(SDPI, r1 - r);
-      const uint8_t* st = acquire();
-      if (!ctl->abort) {
-        for (int rr = cw; rr < nr; rr += NCW) {
-          const uint8_t* row = st + (size_t)rr * L.SDR;
-          for (int tc = 0; tc < T; tc += TK) {
-            const int nt = min(TK, T - tc);
-            float rs[TK];
-#pragma unroll
-            for (int tt = 0; tt < TK; ++tt) rs[tt] = 0.f;
-            for (int cc = lane; cc < Is / 16; cc += 32) {
-              const uint4 cw4 = *reinterpret_cast<const uint4*>(row + cc * 16);
-              const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + Is + (cc >> 2) * 4));
-              float2 q0[4], q1[4];
-              unpack_int8_pair(cw4.x, cw4.y, q0);
-              unpack_int8_pair(cw4.z, cw4.w, q1);
-#pragma unroll
-              for (int tt = 0; tt < TK; ++tt) {
-                if (tt < nt) {
-                  const float4* hv = reinterpret_cast<const float4*>(hsp + (size_t)(tc + tt) * Is + cc * 16);
-                  const float4 A = hv[0], B = hv[1], C = hv[2], D = hv[3];
-                  float2 acc = make_float2(0.f, 0.f);
-                  acc = __ffma2_rn(q0[0], make_float2(A.x, A.y), acc);
-                  acc = __ffma2_rn(q0[1], make_float2(A.z, A.w), acc);
-                  acc = __ffma2_rn(q0[2], make_float2(B.x, B.y), acc);
-                  acc = __ffma2_rn(q0[3], make_float2(B.z, B.w), acc);
-                  acc = __ffma2_rn(q1[0], make_float2(C.x, C.y), acc);
-                  acc = __ffma2_rn(q1[1], make_float2(C.z, C.w), acc);
-                  acc = __ffma2_rn(q1[2], make_float2(D.x, D.y), acc);
-                  acc = __ffma2_rn(q1[3], make_float2(D.z, D.w), acc);
-                  rs[tt] += sb.x * (acc.x + acc.y) + sb.y * hss[(tc + tt) * (Is / 16) + cc];
-                }
-              }
-            }
-#pragma unroll
-            for (int tt = 0; tt < TK; ++tt) rs[tt] = warp_sum(rs[tt]);
-            if (lane == 0)
-              for (int tt = 0; tt < nt; ++tt) shs[(tc + tt) * (r1 - r0) + (r + rr - r0)] = rs[tt];
-          }
-        }
-      }
-      release();
-    }
-    named_bar(BAR_C, CT);
+    if (ctid == 0) stamp(a, 8);
 
     // ---- D: all partials finished -> fixed-order reduction of this CTA's rows
     if (ctid == 0) {
       __threadfence();
       atomicAdd(&a.counters[2], 1u);
       if (!ctl->abort && !spin_geq(&a.counters[2], (uint32_t)G, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_PARTIAL);
+      stamp(a, 11);
     }
     named_bar(BAR_C, CT);
-    __threadfence();
     if (!ctl->abort) {
       const int nr = r1 - r0;
-      const int U = ctl->U;
-      const int N = U * I;
+#pragma unroll 1
       for (int pi = cw; pi < T * nr; pi += NCW) {
         const int t = pi / nr, rr = pi % nr, row = r0 + rr;
         float acc = 0.f;
-        for (int c = lane; c < G; c += 32) {
-          const int lo = range_lo(N, c, G), hi = range_lo(N, c + 1, G);
-          if (lo >= hi) continue;
-          const int a0 = lo / I;
-          for (int aa = a0; aa * I < hi && aa - a0 < DEC_MAXSEG; ++aa) {
-            const uint32_t msk = ctl->act_mask[aa];
-            if (msk & (1u << t)) {
-              const int tl = __popc(msk & ((1u << t) - 1u));
-              const size_t slot = ((size_t)c * DEC_MAXSEG + (aa - a0)) * T + tl;
-              acc += __ldcg(a.partial + slot * H + row);
+#pragma unroll
+        for (int k = 0; k < DEC_MAXGRID / 32; ++k) {
+          const int c = lane + 32 * k;
+          if (c < G) {
+            const int a0 = ctl->tab_a0[c], ns = ctl->tab_n[c];
+#pragma unroll
+            for (int sg = 0; sg < DEC_MAXSEG; ++sg) {
+              if (sg < ns) {
+                const uint32_t msk = ctl->act_mask[a0 + sg];
+                if (msk & (1u << t)) {
+                  const int tl = __popc(msk & ((1u << t) - 1u));
+                  const size_t slot = ((size_t)c * DEC_MAXSEG + sg) * T + tl;
+                  acc += __ldcg(a.partial + slot * H + row);
+                }
+              }
             }
           }
         }
@@ -745,6 +879,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(MoeLayout L, DecodeAr
 
   __syncthreads();
   if (threadIdx.x == 0) {
+    stamp(a, 12);
     __threadfence();
     const uint32_t prev = atomicAdd(&a.counters[3], 1u);
     if (prev == (uint32_t)G - 1) {
@@ -759,6 +894,7 @@ template <int H>
 int hseg_bound(const MoeLayout& L, int T, int grid) {
   int best = 0;
   const int TK = T * L.K;
+#pragma unroll 1
   for (int n = 1; n <= T; ++n) {
     long long U = (long long)TK - n + 1;
     if (U > L.E) U = L.E;
@@ -777,6 +913,7 @@ size_t decode_partial_floats(const MoeLayout& L, int grid, int T) {
 }
 
 bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch* out) {
+  if (grid > DEC_MAXGRID) return false;
   DecodeLaunch pl;
   pl.grid = grid;
   pl.hseg_floats = hseg_bound<0>(L, T, grid);
@@ -798,11 +935,17 @@ bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch
   return true;
 }
 
-template <int H, int TK>
-static cudaError_t launch_h(const MoeLayout& L, const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st) {
-  auto kern = k_decode<H, TK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
-  if (e != cudaSuccess) return e;
+template <class SH, int TK>
+static cudaError_t launch_s(const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st) {
+  auto kern = k_decode<SH, TK>;
+  // raise the dynamic shared-memory limit once per process and instantiation (a per-function setting)
+  static int configured = 0;
+  if (configured < pl.smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    if (e != cudaSuccess) return e;
+    configured = pl.smem > 232448 ? pl.smem : 232448;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(DEC_THREADS);
@@ -813,17 +956,21 @@ static cudaError_t launch_h(const MoeLayout& L, const DecodeArgs& a, const Decod
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, L, a, pl.NS, pl.SS, pl.hseg_floats);
+  return cudaLaunchKernelEx(&cfg, kern, a, pl.NS, pl.SS, pl.hseg_floats);
 }
+
+template <class SH>
+static bool is_shape(const MoeLayout& L) {
+  return L.H == SH::H && L.E == SH::E && L.K == SH::K && L.I == SH::I && L.Is == SH::Is;
+}
+
+bool decode_supported(const MoeLayout& L) { return is_shape<ShapeProd>(L) || is_shape<ShapeTiny>(L); }
 
 cudaError_t decode_launch(const MoeLayout& L, const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st) {
   const bool small = a.T == 1;
-  switch (L.H) {
-    case 512: return small ? launch_h<512, 1>(L, a, pl, st) : launch_h<512, 2>(L, a, pl, st);
-    case 1024: return small ? launch_h<1024, 1>(L, a, pl, st) : launch_h<1024, 2>(L, a, pl, st);
-    case 2048: return small ? launch_h<2048, 1>(L, a, pl, st) : launch_h<2048, 2>(L, a, pl, st);
-    default: return cudaErrorInvalidValue;
-  }
+  if (is_shape<ShapeProd>(L)) return small ? launch_s<ShapeProd, 1>(a, pl, st) : launch_s<ShapeProd, 2>(a, pl, st);
+  if (is_shape<ShapeTiny>(L)) return small ? launch_s<ShapeTiny, 1>(a, pl, st) : launch_s<ShapeTiny, 2>(a, pl, st);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace moe

@@ -11,6 +11,7 @@ constexpr int DEC_THREADS = (DEC_NCW + 1) * 32;   // + one producer warp
 constexpr int DEC_TMAX = 16;                      // largest T of the fused decode kernel
 constexpr int DEC_MAXSEG = 4;                     // expert segments one CTA's unit range may touch
 constexpr int DEC_MAXNS = 24;                     // ring stages
+constexpr int DEC_MAXGRID = 256;                  // CTAs (one per SM)
 
 // device error bits
 enum : uint32_t {
@@ -35,6 +36,7 @@ struct DecodeArgs {
   float* rec_sg;            // [T]
   uint64_t timeout_ns;
   int skip_arrive;
+  uint64_t* trace;          // optional [grid][32] globaltimer stamps at phase boundaries (debug)
 };
 
 struct DecodeLaunch {
@@ -43,6 +45,7 @@ struct DecodeLaunch {
 
 // Host: shared-memory plan for a call with T tokens; returns false if it does not fit.
 bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch* out);
+bool decode_supported(const MoeLayout& L);   // shapes with a compiled decode kernel
 cudaError_t decode_launch(const MoeLayout& L, const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st);
 size_t decode_partial_floats(const MoeLayout& L, int grid, int T);
 

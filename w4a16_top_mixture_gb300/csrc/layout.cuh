@@ -3,7 +3,7 @@
 // The canonical layout (see include/moe_block.h) is regrouped at load time so that every unit of work a CTA
 // streams is one contiguous, 16-byte aligned range that a single bulk copy can move into shared memory:
 //
-//   router   [E+1][RR]     row r: int8 codes of the row, permuted (see int8_perm), then H/64 (s,b) fp16 pairs
+//   router   [E+1][RR]     row r: int8 codes of the row, permuted (see moe_int8_perm), then H/64 (s,b) pairs
 //   sh_gu    [Is][SU]      unit i: gate row codes (permuted) | up row codes (permuted) | gate (s,b) | up (s,b)
 //   sh_dn    [H][SDR]      row r: Is int8 codes in natural order | Is/64 (s,b)
 //   ex_gu    [E][I][EU]    unit (e,i): gate row int4 codes | up row int4 codes | gate (s,b) | up (s,b)
@@ -59,9 +59,14 @@ inline MoeLayout moe_make_layout(int H, int E, int K, int I, int Is) {
   return L;
 }
 
-// byte position of int8 column j inside a permuted row
+// byte position of int8 column j inside a permuted row. The 32-column chunk c = l + LW*p, half h (16
+// columns), lands at ((p*2 + h)*LW + l)*16 so that the lanes of a warp read consecutive 16 bytes; inside each
+// 8-byte block the columns are ordered 0 1 4 5 2 3 6 7, so that the byte pairs (0,2) and (1,3) of each 32-bit
+// word hold the columns (k, 4+k) that the int4 rows also pair.
 MOE_HD int moe_int8_perm(int j, int LW) {
   int c = j >> 5, within = j & 31, h = within >> 4, b = within & 15;
   int l = c % LW, p = c / LW;
-  return ((p * 2 + h) * LW + l) * 16 + b;
+  int blk = b >> 3, k = b & 7;
+  const int pos8[8] = {0, 1, 4, 5, 2, 3, 6, 7};
+  return ((p * 2 + h) * LW + l) * 16 + blk * 8 + pos8[k];
 }

@@ -102,26 +102,29 @@ __global__ void k_debug_dequant(const uint8_t* __restrict__ base, MoeLayout L, i
       size_t sb_off;
       if (which == 0) { row = base + (size_t)r * L.RR; sb_off = L.H; }
       else { row = base + (size_t)r * L.SU + (which == 5 ? L.H : 0); sb_off = 2 * (size_t)L.H - (which == 5 ? L.H : 0) + (which == 5 ? (size_t)L.GB * 4 : 0); }
-      uint32_t w0 = *reinterpret_cast<const uint32_t*>(row + moe_int8_perm(c8, L.LW));
-      uint32_t w1 = *reinterpret_cast<const uint32_t*>(row + moe_int8_perm(c8 + 4, L.LW));
-      float2 q[4];
-      unpack_int8_pair(w0, w1, q);
+      // the 8-byte block of columns c8..c8+7 starts at the permuted position of column c8
+      const uint8_t* blk = row + moe_int8_perm(c8, L.LW);
+      uint32_t pr[4];
+      int8_block_pairs(*reinterpret_cast<const uint32_t*>(blk), *reinterpret_cast<const uint32_t*>(blk + 4), pr);
       float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + sb_off + (c8 / 64) * 4));
       for (int k = 0; k < 4; ++k) {
-        v[k] = __fmaf_rn(sb.x, q[k].x, sb.y);
-        v[4 + k] = __fmaf_rn(sb.x, q[k].y, sb.y);
+        const float2 f = h2f(pr[k]);   // (1024 + c_k, 1024 + c_{4+k}) exactly
+        v[k] = __fmaf_rn(sb.x, f.x - 1024.0f, sb.y);
+        v[4 + k] = __fmaf_rn(sb.x, f.y - 1024.0f, sb.y);
       }
     } else if (which == 1 || which == 2) {
       const uint8_t* unit = base + ((size_t)index * L.I + r) * L.EU;
       const uint8_t* row = unit + (which == 2 ? L.H / 2 : 0);
       size_t sb_off = (size_t)L.H + (which == 2 ? (size_t)L.GB * 4 : 0);
       uint32_t w = *reinterpret_cast<const uint32_t*>(row + c8 / 2);
-      float2 q[4];
-      unpack_int4_word(w, q);
+      uint32_t pr[4];
+      int4_word_pairs(w, pr);
       float2 sb = h2f(*reinterpret_cast<const uint32_t*>(unit + sb_off + (c8 / 64) * 4));
       for (int k = 0; k < 4; ++k) {
-        v[k] = __fmaf_rn(sb.x, q[k].x, sb.y);
-        v[4 + k] = __fmaf_rn(sb.x, q[k].y, sb.y);
+        const float2 f = h2f(pr[k]);   // 1024 + q (k even) or 1024 + 16 q (k odd), exactly
+        const float sc = (k & 1) ? 0.0625f : 1.0f;
+        v[k] = __fmaf_rn(sb.x, (f.x - 1024.0f) * sc, sb.y);
+        v[4 + k] = __fmaf_rn(sb.x, (f.y - 1024.0f) * sc, sb.y);
       }
     } else if (which == 3) {
       // row r of the down matrix: column c of group g sits in block (index, g), unit c%64, quad r/4
@@ -140,11 +143,12 @@ __global__ void k_debug_dequant(const uint8_t* __restrict__ base, MoeLayout L, i
       uint32_t w0 = *reinterpret_cast<const uint32_t*>(row + c8);
       uint32_t w1 = *reinterpret_cast<const uint32_t*>(row + c8 + 4);
       float2 q[4];
-      unpack_int8_pair(w0, w1, q);
+      unpack_int8_word(w0, q[0], q[1]);
+      unpack_int8_word(w1, q[2], q[3]);
       float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + L.Is + (c8 / 64) * 4));
       for (int k = 0; k < 4; ++k) {
-        v[k] = __fmaf_rn(sb.x, q[k].x, sb.y);
-        v[4 + k] = __fmaf_rn(sb.x, q[k].y, sb.y);
+        v[2 * k] = __fmaf_rn(sb.x, q[k].x, sb.y);
+        v[2 * k + 1] = __fmaf_rn(sb.x, q[k].y, sb.y);
       }
     }
     float* o = out + (size_t)r * cols + c8;

@@ -22,7 +22,7 @@ WEIGHT_FIELDS = [
 EXPORTS = ["moe_block_create", "moe_block_load_weights", "moe_block_forward", "moe_block_forward_host",
            "moe_block_forward_residual", "moe_block_get_status", "moe_block_destroy", "moe_block_strerror",
            "moe_last_cuda_error", "moe_block_debug_dequant", "moe_block_debug_last_routing",
-           "moe_block_debug_set_wait", "moe_block_last_launch_count"]
+           "moe_block_debug_set_wait", "moe_block_debug_set_trace", "moe_block_last_launch_count"]
 
 
 class MoeError(RuntimeError):
@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_block_debug_last_routing.argtypes = [vp, i, vp, vp, vp, vp, vp]
     lib.moe_block_debug_set_wait.argtypes = [vp, u32, i]
     lib.moe_block_last_launch_count.argtypes = [vp]
+    lib.moe_block_debug_set_trace.argtypes = [vp, vp]
     for n in EXPORTS:
         if not hasattr(lib, n):
             raise RuntimeError(f"{path} does not export {n}")
@@ -208,6 +209,10 @@ class MoeBlock:
 
     def set_wait(self, timeout_us=0, skip_arrive=False):
         _check(self.lib.moe_block_debug_set_wait(self.h, int(timeout_us), int(bool(skip_arrive))), "set_wait")
+
+    def set_trace(self, buf=None):
+        """buf: int64 CUDA tensor of >= 32 * SM-count entries, or None to stop tracing."""
+        _check(self.lib.moe_block_debug_set_trace(self.h, _ptr(buf)), "set_trace")
 
     def last_launch_count(self):
         return self.lib.moe_block_last_launch_count(self.h)

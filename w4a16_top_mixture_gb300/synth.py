@@ -178,6 +178,11 @@ def zipf_router(cfg: BlockConfig, x: np.ndarray, seed: int, layer: int = 0, s_ex
     return (np.concatenate([q, sq[E:]], 0), np.concatenate([s, ss[E:]], 0), np.concatenate([b, sb[E:]], 0))
 
 
+def layer_bytes(cfg: BlockConfig) -> int:
+    """All weight + scale/bias bytes of one block (every expert)."""
+    return unique_weight_bytes(cfg, cfg.n_experts)
+
+
 def unique_weight_bytes(cfg: BlockConfig, n_unique_experts: int) -> int:
     """Weight + scale/bias bytes one call must read: router, shared expert and each selected expert once."""
     H, I, Is, E, G = cfg.hidden, cfg.expert_inter, cfg.shared_inter, cfg.n_experts, cfg.group
