@@ -134,6 +134,21 @@ MOE_API int moe_block_debug_set_wait(moe_block_t *blk, uint32_t timeout_us, int 
  * memory of at least 32 * number-of-SMs entries, caller-owned); NULL switches tracing off. */
 MOE_API int moe_block_debug_set_trace(moe_block_t *blk, void *trace_device);
 
+/* ---- allocation-free routing ----
+ * No counterpart on the pages: a convenience for callers that may not allocate device memory when they call
+ * (inside CUDA stream capture, where cudaMalloc is illegal, or under a runtime whose allocator must own every
+ * device byte). Computes the routing step of the block -- router logits from the CANONICAL int8 router
+ * (router_q [E+1][H], router_s/b [E+1][H/64] fp16 bits, device memory), softmax over the E expert logits,
+ * top-k, renormalisation, sigmoid of the shared-gate logit -- for x [T][H] fp16 (device) into ids [T][k] int32
+ * (ascending), weights [T][k] fp32 and sgate [T] fp32 (device). It allocates nothing: the logits live in a
+ * fixed 131 KB device array inside the library (T <= 64 tokens, E <= 512 experts; larger T or E return
+ * MOE_ERR_INVALID_ARG). Every call shares that array, so calls that overlap on the GPU (other streams, other
+ * threads) race and must be serialised by the caller. The first call on a device looks up the array's device
+ * address once; make that first call before any stream capture. Asynchronous on `stream`. */
+MOE_API int moe_router_topk_noalloc(const uint8_t *router_q, const uint16_t *router_s, const uint16_t *router_b,
+                                    int hidden, int n_experts, int top_k, const void *x, int T, int32_t *ids,
+                                    float *weights, float *sgate, void *stream);
+
 /* Number of CUDA kernel launches the last forward call made. */
 MOE_API int moe_block_last_launch_count(moe_block_t *blk);
 

@@ -22,7 +22,8 @@ WEIGHT_FIELDS = [
 EXPORTS = ["moe_block_create", "moe_block_load_weights", "moe_block_forward", "moe_block_forward_host",
            "moe_block_forward_residual", "moe_block_get_status", "moe_block_destroy", "moe_block_strerror",
            "moe_last_cuda_error", "moe_block_debug_dequant", "moe_block_debug_last_routing",
-           "moe_block_debug_set_wait", "moe_block_debug_set_trace", "moe_block_last_launch_count"]
+           "moe_block_debug_set_wait", "moe_block_debug_set_trace", "moe_block_last_launch_count",
+           "moe_router_topk_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -75,6 +76,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_block_debug_set_wait.argtypes = [vp, u32, i]
     lib.moe_block_last_launch_count.argtypes = [vp]
     lib.moe_block_debug_set_trace.argtypes = [vp, vp]
+    lib.moe_router_topk_noalloc.argtypes = [vp, vp, vp, i, i, i, vp, i, vp, vp, vp, vp]
     for n in EXPORTS:
         if not hasattr(lib, n):
             raise RuntimeError(f"{path} does not export {n}")
