@@ -28,7 +28,9 @@ namespace {
 
 constexpr int NCW = DEC_NCW;
 constexpr int CT = NCW * 32;   // consumer threads
-constexpr int BAR_C = 1;       // named barrier of the consumer warps
+constexpr int BAR_C = 1;       // named barrier of all consumer warps
+constexpr int BAR_A = 2;       // the shared-expert team
+constexpr int BAR_R = 3;       // the routing team
 constexpr uint32_t FULL = 0xFFFFFFFFu;
 
 constexpr size_t c_align16(size_t v) { return (v + 15) & ~(size_t)15; }
@@ -67,6 +69,7 @@ struct Ctl {
   int ids[DEC_TMAX][16];
   float wts[DEC_TMAX][16];
   float sg[DEC_TMAX];
+  float rn[DEC_TMAX];
   uint32_t emask[512];
   uint16_t act_e[512];
   uint32_t act_mask[512];
@@ -113,6 +116,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ void stamp(const DecodeArgs& a, int slot) {
   if (a.trace) a.trace[blockIdx.x * 32 + slot] = globaltimer();
+}
+// per-warp stamps (lane 0): trace[grid*32 + (cta*16 + warp)*4 + k]
+__device__ __forceinline__ void wstamp(const DecodeArgs& a, int cw, int k) {
+  if (a.trace && (threadIdx.x & 31) == 0) a.trace[gridDim.x * 32 + (blockIdx.x * 16 + cw) * 4 + k] = globaltimer();
 }
 
 __device__ __forceinline__ void set_error(const DecodeArgs& a, Ctl* ctl, uint32_t bit) {
@@ -394,11 +401,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       if (++cs == NS) { cs = 0; cph ^= 1u; }
     };
 
-    // ---- x prologue: (RMSNorm ->) fp16 activations in pair order, plus per-chunk pair-column sums
-    for (int t = cw; t < T; t += NCW) {
-      const uint16_t* xr = a.x + (size_t)t * H;
-      float rn = 1.f;
-      if (a.gamma) {
+    // ---- x prologue: (RMSNorm ->) fp16 activations in pair order, plus per-chunk pair-column sums; one
+    // (token, 32-column chunk) item per consumer thread
+    if (a.gamma) {
+#pragma unroll 1
+      for (int t = cw; t < T; t += NCW) {
+        const uint16_t* xr = a.x + (size_t)t * H;
         float ss = 0.f;
 #pragma unroll 1
         for (int i = lane * 8; i < H; i += 256) {
@@ -411,40 +419,40 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
           }
         }
         ss = warp_sum(ss);
-        rn = 1.0f / sqrtf(ss / (float)H + a.eps);
+        if (lane == 0) ctl->rn[t] = 1.0f / sqrtf(ss / (float)H + a.eps);
       }
-      if (lane < LW) {
+      named_bar(BAR_C, CT);
+    }
 #pragma unroll 1
-        for (int p = 0; p < P; ++p) {
-          const int c = lane + LW * p;
-          uint4 raw[4];
+    for (int item = ctid; item < T * NCH; item += CT) {
+      const int t = item / NCH, c = item % NCH, l = c % LW, p = c / LW;
+      const uint16_t* xr = a.x + (size_t)t * H + c * 32;
+      uint4 raw[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) raw[j] = *reinterpret_cast<const uint4*>(xr + c * 32 + j * 8);
-          float xl = 0.f, xhs = 0.f;
+      for (int j = 0; j < 4; ++j) raw[j] = *reinterpret_cast<const uint4*>(xr + j * 8);
+      const float rn = a.gamma ? ctl->rn[t] : 1.f;
+      float xl = 0.f, xhs = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            __half h8[8];
-            *reinterpret_cast<uint4*>(h8) = raw[j];
-            if (a.gamma) {
-              const uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + c * 32 + j * 8);
-              const __half* g8 = reinterpret_cast<const __half*>(&graw);
+      for (int j = 0; j < 4; ++j) {
+        __half h8[8];
+        *reinterpret_cast<uint4*>(h8) = raw[j];
+        if (a.gamma) {
+          const uint4 graw = *reinterpret_cast<const uint4*>(a.gamma + c * 32 + j * 8);
+          const __half* g8 = reinterpret_cast<const __half*>(&graw);
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                h8[k] = __float2half_rn(__half2float(h8[k]) * rn * __half2float(g8[k]));
-            }
-            // pair order (0,4) (1,5) (2,6) (3,7); "low" columns 0 4 2 6, "high" columns 1 5 3 7
-            uint4 o;
-            o.x = (uint32_t)__half_as_ushort(h8[0]) | ((uint32_t)__half_as_ushort(h8[4]) << 16);
-            o.y = (uint32_t)__half_as_ushort(h8[1]) | ((uint32_t)__half_as_ushort(h8[5]) << 16);
-            o.z = (uint32_t)__half_as_ushort(h8[2]) | ((uint32_t)__half_as_ushort(h8[6]) << 16);
-            o.w = (uint32_t)__half_as_ushort(h8[3]) | ((uint32_t)__half_as_ushort(h8[7]) << 16);
-            xh[((t * P + p) * 4 + j) * LW + lane] = o;
-            xl += (__half2float(h8[0]) + __half2float(h8[4])) + (__half2float(h8[2]) + __half2float(h8[6]));
-            xhs += (__half2float(h8[1]) + __half2float(h8[5])) + (__half2float(h8[3]) + __half2float(h8[7]));
-          }
-          xs[(t * P + p) * LW + lane] = make_float2(xl, xhs);
+          for (int k = 0; k < 8; ++k) h8[k] = __float2half_rn(__half2float(h8[k]) * rn * __half2float(g8[k]));
         }
+        // pair order (0,4) (1,5) (2,6) (3,7); "low" columns 0 4 2 6, "high" columns 1 5 3 7
+        uint4 o;
+        o.x = (uint32_t)__half_as_ushort(h8[0]) | ((uint32_t)__half_as_ushort(h8[4]) << 16);
+        o.y = (uint32_t)__half_as_ushort(h8[1]) | ((uint32_t)__half_as_ushort(h8[5]) << 16);
+        o.z = (uint32_t)__half_as_ushort(h8[2]) | ((uint32_t)__half_as_ushort(h8[6]) << 16);
+        o.w = (uint32_t)__half_as_ushort(h8[3]) | ((uint32_t)__half_as_ushort(h8[7]) << 16);
+        xh[((t * P + p) * 4 + j) * LW + l] = o;
+        xl += (__half2float(h8[0]) + __half2float(h8[4])) + (__half2float(h8[2]) + __half2float(h8[6]));
+        xhs += (__half2float(h8[1]) + __half2float(h8[5])) + (__half2float(h8[3]) + __half2float(h8[7]));
       }
+      xs[(t * P + p) * LW + l] = make_float2(xl, xhs);
     }
     named_bar(BAR_C, CT);
     if (ctid == 0) stamp(a, 1);
@@ -454,7 +462,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       const int nr = min(RPI, rb - r);
       const uint8_t* st = acquire();
       if (!ctl->abort) {
-        for (int rr = cw; rr < nr; rr += NCW) {
+        const int rbase = r - ra;
+#pragma unroll 1
+        for (int rr = (cw - rbase % NCW + NCW) % NCW; rr < nr; rr += NCW) {
           const uint8_t* b0 = st + (size_t)rr * L.RR;
           for (int tc = 0; tc < T; tc += TK) {
             const int nt = min(TK, T - tc);
@@ -478,118 +488,133 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       }
     }
 
-    // ---- A2: shared-expert gate/up units, a pair per warp (overlaps the wait for every CTA's logits)
+    // The warps split in two teams: RW routing warps wait for every CTA's logits and route, while the other AW
+    // warps compute this CTA's shared-expert gate/up units; both join again before the shared down rows.
+    const int RW = T < 8 ? T : 8, AW = NCW - RW;
+    if (cw < AW) {
+      // ---- A2: shared-expert gate/up units, a pair per warp
 #pragma unroll 1
-    for (int u = sa; u < sbn; u += SPI) {
-      const int nu = min(SPI, sbn - u);
-      const uint8_t* st = acquire();
-      if (!ctl->abort) {
+      for (int u = sa; u < sbn; u += SPI) {
+        const int nu = min(SPI, sbn - u);
+        const uint8_t* st = acquire();
+        if (!ctl->abort) {
+          const int pbase = (u - sa) >> 1;
 #pragma unroll 1
-        for (int pr = cw; pr * 2 < nu; pr += NCW) {
-          const uint8_t* ub = st + (size_t)(2 * pr) * L.SU;
-          const int nvalid = (2 * pr + 1 < nu) ? 4 : 2;
-          const int i0 = u + 2 * pr;
+          for (int pr = (cw - pbase % AW + AW) % AW; pr * 2 < nu; pr += AW) {
+            const uint8_t* ub = st + (size_t)(2 * pr) * L.SU;
+            const int nvalid = (2 * pr + 1 < nu) ? 4 : 2;
+            const int i0 = u + 2 * pr;
 #pragma unroll 1
-          for (int tc = 0; tc < T; tc += TK) {
-            const int nt = min(TK, T - tc);
-            const DotR<4, TK> d = dot_rows<H, 4, TK, true>(ub, ub + H, ub + L.SU, ub + L.SU + H, ub + 2 * H,
-                                                           ub + 2 * H + L.GB * 4, ub + L.SU + 2 * H,
-                                                           ub + L.SU + 2 * H + L.GB * 4, nvalid, xh, xs, tc, tc + TK - 1,
-                                                           nt);
-            if (lane < 2 * TK) {
-              const int tt = lane >> 1, k = lane & 1;
-              float g = 0.f, up = 0.f;
+            for (int tc = 0; tc < T; tc += TK) {
+              const int nt = min(TK, T - tc);
+              const DotR<4, TK> d = dot_rows<H, 4, TK, true>(ub, ub + H, ub + L.SU, ub + L.SU + H, ub + 2 * H,
+                                                             ub + 2 * H + L.GB * 4, ub + L.SU + 2 * H,
+                                                             ub + L.SU + 2 * H + L.GB * 4, nvalid, xh, xs, tc,
+                                                             tc + TK - 1, nt);
+              if (lane < 2 * TK) {
+                const int tt = lane >> 1, k = lane & 1;
+                float g = 0.f, up = 0.f;
 #pragma unroll
-              for (int q = 0; q < TK; ++q)
-                if (q == tt) { g = k ? d.v[q][2] : d.v[q][0]; up = k ? d.v[q][3] : d.v[q][1]; }
-              if (tt < nt && 2 * k < nvalid) a.hs[(size_t)(tc + tt) * Is + i0 + k] = silu_fast(g) * up;
+                for (int q = 0; q < TK; ++q)
+                  if (q == tt) { g = k ? d.v[q][2] : d.v[q][0]; up = k ? d.v[q][3] : d.v[q][1]; }
+                if (tt < nt && 2 * k < nvalid) a.hs[(size_t)(tc + tt) * Is + i0 + k] = silu_fast(g) * up;
+              }
             }
           }
         }
+        release();
       }
-      release();
-    }
-    named_bar(BAR_C, CT);
-    if (ctid == 0) {
-      __threadfence();
-      atomicAdd(&a.counters[1], 1u);
-      stamp(a, 6);
-    }
-
-    // ---- R: routing (every CTA, every token)
-    if (ctid == 0 && !ctl->abort && !spin_geq(&a.counters[0], (uint32_t)G, a.timeout_ns))
-      set_error(a, ctl, ERR_WAIT_LOGITS);
-    if (ctid == 0) stamp(a, 3);
-    named_bar(BAR_C, CT);
-    if (!ctl->abort) {
-#pragma unroll 1
-      for (int t = cw; t < T; t += NCW) {
-        const float* lg = a.logits + (size_t)t * (E + 1);
-        int my_idx;
-        float my_logit;
-        warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit);
-        const float mx = __shfl_sync(FULL, my_logit, 0);
-        const float ex = lane < K ? expf(my_logit - mx) : 0.f;
-        const float Z = warp_sum(ex);
-        int rank = 0;
-#pragma unroll 1
-        for (int i = 0; i < K; ++i) {
-          const int oi = __shfl_sync(FULL, my_idx, i);
-          rank += (oi < my_idx) ? 1 : 0;
-        }
-        if (lane < K) {
-          ctl->ids[t][rank] = my_idx;
-          ctl->wts[t][rank] = ex / Z;
-        }
-        if (lane == 0) {
-          const float g = __ldcg(lg + E);
-          ctl->sg[t] = 1.0f / (1.0f + expf(-g));
-        }
+      named_bar(BAR_A, AW * 32);
+      if (ctid == 0) {
+        __threadfence();
+        atomicAdd(&a.counters[1], 1u);
+        stamp(a, 6);
       }
-    }
-    named_bar(BAR_C, CT);
-    if (ctid == 0) stamp(a, 4);
-    // bucketing: token masks per expert, active experts in ascending order
-    if (T == 1) {
-      if (ctid < K) {
-        ctl->act_e[ctid] = (uint16_t)ctl->ids[0][ctid];
-        ctl->act_mask[ctid] = 1u;
-      }
-      if (ctid == 0) ctl->U = ctl->abort ? 0 : K;
     } else {
+      const int rt = cw - AW, rtid = ctid - AW * 32, NT = RW * 32;
+      // this team does not read the shared-expert items: it only counts itself out of their stages
 #pragma unroll 1
-      for (int e = ctid; e < E; e += CT) ctl->emask[e] = 0u;
-      named_bar(BAR_C, CT);
-      if (!ctl->abort)
+      for (int u = sa; u < sbn; u += SPI) release();
+      // ---- R: routing (every CTA, every token)
+      if (rtid == 0 && !ctl->abort && !spin_geq(&a.counters[0], (uint32_t)G, a.timeout_ns))
+        set_error(a, ctl, ERR_WAIT_LOGITS);
+      if (rtid == 0) stamp(a, 3);
+      named_bar(BAR_R, NT);
+      if (!ctl->abort) {
 #pragma unroll 1
-        for (int p = ctid; p < T * K; p += CT) atomicOr(&ctl->emask[ctl->ids[p / K][p % K]], 1u << (p / K));
-      named_bar(BAR_C, CT);
-      const uint32_t msk = ctid < E ? ctl->emask[ctid] : 0u;
-      const uint32_t bal = __ballot_sync(FULL, msk != 0u);
-      if (lane == 0) ctl->warp_tot[cw] = __popc(bal);
-      named_bar(BAR_C, CT);
-      int base = 0;
-#pragma unroll 1
-      for (int w = 0; w < cw; ++w) base += ctl->warp_tot[w];
-      if (msk != 0u) {
-        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-        ctl->act_e[pos] = (uint16_t)ctid;
-        ctl->act_mask[pos] = msk;
+        for (int t = rt; t < T; t += RW) {
+          const float* lg = a.logits + (size_t)t * (E + 1);
+          int my_idx;
+          float my_logit;
+          warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit);
+          const float mx = __shfl_sync(FULL, my_logit, 0);
+          const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
+          const float Z = warp_sum(ex);
+          int rank = 0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int oi = __shfl_sync(FULL, my_idx, i);
+            rank += (i < K && oi < my_idx) ? 1 : 0;
+          }
+          if (lane < K) {
+            ctl->ids[t][rank] = my_idx;
+            ctl->wts[t][rank] = __fdividef(ex, Z);
+          }
+          if (lane == 0) ctl->sg[t] = __frcp_rn(1.0f + __expf(-__ldcg(lg + E)));
+        }
       }
-      if (ctid == CT - 1) ctl->U = base + __popc(bal);
-    }
-    named_bar(BAR_C, CT);
-    {
+      named_bar(BAR_R, NT);
+      if (rtid == 0) stamp(a, 4);
+      // bucketing: token masks per expert, active experts in ascending order
+      if (T == 1) {
+        if (rtid < K) {
+          ctl->act_e[rtid] = (uint16_t)ctl->ids[0][rtid];
+          ctl->act_mask[rtid] = 1u;
+        }
+        if (rtid == 0) ctl->U = ctl->abort ? 0 : K;
+      } else {
+#pragma unroll 1
+        for (int e = rtid; e < E; e += NT) ctl->emask[e] = 0u;
+        named_bar(BAR_R, NT);
+        if (!ctl->abort)
+#pragma unroll 1
+          for (int p = rtid; p < T * K; p += NT) atomicOr(&ctl->emask[ctl->ids[p / K][p % K]], 1u << (p / K));
+        named_bar(BAR_R, NT);
+        const int EPT = (E + NT - 1) / NT;
+        int cnt = 0;
+#pragma unroll 1
+        for (int q = 0; q < EPT; ++q) {
+          const int e = rtid * EPT + q;
+          cnt += (e < E && ctl->emask[e] != 0u) ? 1 : 0;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(FULL, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (lane == 31) ctl->warp_tot[rt] = incl;
+        named_bar(BAR_R, NT);
+        int base = 0;
+#pragma unroll 1
+        for (int w = 0; w < rt; ++w) base += ctl->warp_tot[w];
+        int pos = base + incl - cnt;
+#pragma unroll 1
+        for (int q = 0; q < EPT; ++q) {
+          const int e = rtid * EPT + q;
+          const uint32_t msk = e < E ? ctl->emask[e] : 0u;
+          if (msk != 0u) {
+            ctl->act_e[pos] = (uint16_t)e;
+            ctl->act_mask[pos] = msk;
+            ++pos;
+          }
+        }
+        if (rtid == NT - 1) ctl->U = base + incl;
+      }
+      named_bar(BAR_R, NT);
       const int U = ctl->U;
       const int N = U * I;
-      // segment table of every CTA (for the final reduction)
-#pragma unroll 1
-      for (int c = ctid; c < G; c += CT) {
-        const int lo = range_lo(N, c, G), hi = range_lo(N, c + 1, G);
-        ctl->tab_a0[c] = (uint16_t)(lo / I);
-        ctl->tab_n[c] = (uint8_t)(lo < hi ? (hi - 1) / I - lo / I + 1 : 0);
-      }
-      if (ctid == 0) {
+      if (rtid == 0) {
         const int lo = range_lo(N, cta, G), hi = range_lo(N, cta + 1, G);
         int nseg = 0;
 #pragma unroll 1
@@ -621,17 +646,22 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
         ctl->nseg = ctl->abort ? 0 : nseg;
         mbar_arrive(&ctl->route_ready);
         stamp(a, 5);
-        if (cta == 0 && a.rec_ids) {
+      }
+      // off the critical path: every CTA's segment table (final reduction) and the routing record
 #pragma unroll 1
-          for (int t = 0; t < T; ++t) {
+      for (int c = rtid; c < G; c += NT) {
+        const int lo = range_lo(N, c, G), hi = range_lo(N, c + 1, G);
+        ctl->tab_a0[c] = (uint16_t)(lo / I);
+        ctl->tab_n[c] = (uint8_t)(lo < hi ? (hi - 1) / I - lo / I + 1 : 0);
+      }
+      if (cta == 0 && a.rec_ids) {
 #pragma unroll 1
-            for (int j = 0; j < K; ++j) {
-              a.rec_ids[t * K + j] = ctl->ids[t][j];
-              a.rec_w[t * K + j] = ctl->wts[t][j];
-            }
-            a.rec_sg[t] = ctl->sg[t];
-          }
+        for (int p = rtid; p < T * K; p += NT) {
+          a.rec_ids[p] = ctl->ids[p / K][p % K];
+          a.rec_w[p] = ctl->wts[p / K][p % K];
         }
+#pragma unroll 1
+        for (int t = rtid; t < T; t += NT) a.rec_sg[t] = ctl->sg[t];
       }
     }
     named_bar(BAR_C, CT);
@@ -714,13 +744,17 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       const int units = u1 - u0;
       const uint8_t* toks = ctl->seg_tok[sgi];
       // gate/up -> h, a pair of units per warp
+      if (sgi == 0) wstamp(a, cw, 0);
 #pragma unroll 1
       for (int u = u0; u < u1; u += UPI) {
         const int nu = min(UPI, u1 - u);
         const uint8_t* st = acquire();
         if (!ctl->abort) {
+          // pairs are numbered across the whole segment so that consecutive items go to different warps
+          const int pbase = (u - u0) >> 1;
 #pragma unroll 1
-          for (int pr = cw; pr * 2 < nu; pr += NCW) {
+          for (int pr = (cw - pbase % NCW + NCW) % NCW; pr * 2 < nu; pr += NCW) {
+            if (sgi == 0) wstamp(a, cw, 1);
             const uint8_t* ub = st + (size_t)(2 * pr) * L.EU;
             const int nvalid = (2 * pr + 1 < nu) ? 4 : 2;
             const int ul = u + 2 * pr - u0;
@@ -740,12 +774,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
                 if (tt < nt && 2 * k < nvalid) hseg[(tc + tt) * units + ul + k] = silu_fast(g) * up;
               }
             }
+            if (sgi == 0) wstamp(a, cw, 2);
           }
         }
         release();
       }
       named_bar(BAR_C, CT);
       if (ctid == 0 && sgi == 0) stamp(a, 7);
+      if (sgi == 0) wstamp(a, cw, 3);
       // down: per group, the (s,b) block then the unit columns; each thread owns 4 output rows
       const int hq = ctid;
       const bool has_q = hq < H / 4;
@@ -783,7 +819,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
                 hsum[tt] = 0.f;
               }
               const float* hrow = hseg + (size_t)tc * units + (u - u0);
-#pragma unroll 2
+#pragma unroll 4
               for (int k = 0; k < nu; ++k) {
                 const uint32_t hw = *reinterpret_cast<const uint16_t*>(st + (size_t)k * L.DCB + hq * 2);
                 float2 q01, q23;
@@ -847,22 +883,34 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
 #pragma unroll 1
       for (int pi = cw; pi < T * nr; pi += NCW) {
         const int t = pi / nr, rr = pi % nr, row = r0 + rr;
-        float acc = 0.f;
+        // every partial this lane needs is loaded before any is added (independent L2 reads in flight)
+        float v[DEC_MAXGRID / 32][2];
 #pragma unroll
         for (int k = 0; k < DEC_MAXGRID / 32; ++k) {
           const int c = lane + 32 * k;
-          if (c < G) {
-            const int a0 = ctl->tab_a0[c], ns = ctl->tab_n[c];
+          const int a0 = c < G ? ctl->tab_a0[c] : 0, ns = c < G ? ctl->tab_n[c] : 0;
 #pragma unroll
-            for (int sg = 0; sg < DEC_MAXSEG; ++sg) {
-              if (sg < ns) {
-                const uint32_t msk = ctl->act_mask[a0 + sg];
-                if (msk & (1u << t)) {
-                  const int tl = __popc(msk & ((1u << t) - 1u));
-                  const size_t slot = ((size_t)c * DEC_MAXSEG + sg) * T + tl;
-                  acc += __ldcg(a.partial + slot * H + row);
-                }
-              }
+          for (int sg = 0; sg < 2; ++sg) {
+            const uint32_t msk = sg < ns ? ctl->act_mask[a0 + sg] : 0u;
+            const bool use = (msk >> t) & 1u;
+            const int tl = __popc(msk & ((1u << t) - 1u));
+            const size_t slot = ((size_t)c * DEC_MAXSEG + sg) * T + tl;
+            v[k][sg] = use ? __ldcg(a.partial + slot * H + row) : 0.f;
+          }
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < DEC_MAXGRID / 32; ++k) acc += v[k][0] + v[k][1];
+        // rare: a CTA whose unit range touches more than two experts
+#pragma unroll 1
+        for (int c = lane; c < G; c += 32) {
+          const int a0 = ctl->tab_a0[c], ns = ctl->tab_n[c];
+#pragma unroll 1
+          for (int sg = 2; sg < ns; ++sg) {
+            const uint32_t msk = ctl->act_mask[a0 + sg];
+            if ((msk >> t) & 1u) {
+              const int tl = __popc(msk & ((1u << t) - 1u));
+              acc += __ldcg(a.partial + (((size_t)c * DEC_MAXSEG + sg) * T + tl) * H + row);
             }
           }
         }
