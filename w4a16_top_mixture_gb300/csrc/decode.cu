@@ -76,6 +76,8 @@ struct Ctl {
   int warp_tot[NCW];
   uint16_t tab_a0[DEC_MAXGRID];   // per CTA: first active-expert index of its unit range
   uint8_t tab_n[DEC_MAXGRID];     // per CTA: number of segments
+  int nslot[DEC_TMAX];            // per token: number of partial-sum slots holding it
+  uint16_t slot[DEC_TMAX][2 * DEC_MAXGRID];   // per token: the slots, in (CTA, segment) order
 };
 constexpr int CTL_BYTES = (sizeof(Ctl) + 127) & ~127;
 
@@ -228,44 +230,54 @@ __device__ __noinline__ DotR<NR, TK> dot_rows(const uint8_t* r0, const uint8_t* 
 }
 
 // Top-k of one token's expert logits held by a warp. Lane l holds experts l*EPL .. l*EPL+EPL-1 (a lower lane
-// means lower indices) as order-preserving integer keys, sorts them descending with a stable odd-even
-// transposition network (equal keys keep ascending indices), then k rounds take the warp maximum of the lane
-// heads, the lowest lane winning ties, and the winning lane pops its head. Lane j < k returns the j-th largest
-// (index, logit).
+// means lower indices) as order-preserving integer keys. Each of the k rounds takes the warp maximum of the lane
+// maxima (the lowest lane winning ties; within a lane the lowest index), and only the winning lane recomputes
+// its maximum. Lane j < k returns the j-th largest (index, logit).
+// Once the k experts are known, lane j asks L2 to prefetch this CTA's 1/G slice of the j-th one's weights
+// (pf_gu / pf_dn: the expert blocks, pf_gu_sz / pf_dn_sz bytes each): the grid as a whole starts pulling the
+// selected experts into L2 while the bucketing runs, ahead of the weight copies that follow it.
 template <int EPL>
 __device__ __noinline__ void warp_topk(const float* __restrict__ lg, int E, int K, int lane, int& my_idx,
-                                       float& my_logit) {
+                                       float& my_logit, const uint8_t* pf_gu, size_t pf_gu_sz,
+                                       const uint8_t* pf_dn, size_t pf_dn_sz) {
   uint32_t key[EPL];
-  int id[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane * EPL + i;
     const uint32_t b = e < E ? __float_as_uint(__ldcg(lg + e)) : 0u;
     key[i] = e < E ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
-    id[i] = e;
   }
+  uint32_t best = key[0];
+  int bi = 0;
 #pragma unroll
-  for (int ph = 0; ph < EPL; ++ph) {
-#pragma unroll
-    for (int i = ph & 1; i + 1 < EPL; i += 2) {
-      const bool sw = key[i] < key[i + 1];
-      const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
-      const int i0 = sw ? id[i + 1] : id[i], i1 = sw ? id[i] : id[i + 1];
-      key[i] = k0; key[i + 1] = k1; id[i] = i0; id[i + 1] = i1;
-    }
-  }
+  for (int i = 1; i < EPL; ++i)
+    if (key[i] > best) { best = key[i]; bi = i; }
   my_idx = -1;
   uint32_t my_key = 0;
+  const int G = gridDim.x, c = blockIdx.x;
+  const size_t gu0 = ((pf_gu_sz * c / G) & ~(size_t)15), gu1 = ((pf_gu_sz * (c + 1) / G) & ~(size_t)15);
+  const size_t dn0 = ((pf_dn_sz * c / G) & ~(size_t)15), dn1 = ((pf_dn_sz * (c + 1) / G) & ~(size_t)15);
+#pragma unroll 1
   for (int j = 0; j < K; ++j) {
-    const uint32_t m = __reduce_max_sync(FULL, key[0]);
-    const int win = __ffs(__ballot_sync(FULL, key[0] == m)) - 1;
-    const int sel = __shfl_sync(FULL, id[0], win);
+    const uint32_t m = __reduce_max_sync(FULL, best);
+    const int win = __ffs(__ballot_sync(FULL, best == m)) - 1;
+    const int sel = __shfl_sync(FULL, lane * EPL + bi, win);
     if (lane == j) { my_idx = sel; my_key = m; }
     if (lane == win) {
 #pragma unroll
-      for (int i = 0; i + 1 < EPL; ++i) { key[i] = key[i + 1]; id[i] = id[i + 1]; }
-      key[EPL - 1] = 0u;
+      for (int i = 0; i < EPL; ++i)
+        if (i == bi) key[i] = 0u;
+      best = key[0];
+      bi = 0;
+#pragma unroll
+      for (int i = 1; i < EPL; ++i)
+        if (key[i] > best) { best = key[i]; bi = i; }
     }
+  }
+  // lane j < k starts the L2 prefetch of this CTA's slice of the j-th selected expert
+  if (lane < K && pf_gu) {
+    if (gu1 > gu0) prefetch_l2(pf_gu + (size_t)my_idx * pf_gu_sz + gu0, (uint32_t)(gu1 - gu0));
+    if (dn1 > dn0) prefetch_l2(pf_dn + (size_t)my_idx * pf_dn_sz + dn0, (uint32_t)(dn1 - dn0));
   }
   const uint32_t b = (my_key & 0x80000000u) ? (my_key & 0x7FFFFFFFu) : ~my_key;
   my_logit = __uint_as_float(b);
@@ -546,7 +558,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
           const float* lg = a.logits + (size_t)t * (E + 1);
           int my_idx;
           float my_logit;
-          warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit);
+          warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit, a.ex_gu, L.exgu_expert, a.ex_dn,
+                                   L.exdn_expert);
           const float mx = __shfl_sync(FULL, my_logit, 0);
           const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
           const float Z = warp_sum(ex);
@@ -647,13 +660,15 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
         mbar_arrive(&ctl->route_ready);
         stamp(a, 5);
       }
-      // off the critical path: every CTA's segment table (final reduction) and the routing record
+      // off the critical path: every CTA's segment table and, per token, the list of partial-sum slots that
+      // hold it (final reduction)
 #pragma unroll 1
       for (int c = rtid; c < G; c += NT) {
         const int lo = range_lo(N, c, G), hi = range_lo(N, c + 1, G);
         ctl->tab_a0[c] = (uint16_t)(lo / I);
         ctl->tab_n[c] = (uint8_t)(lo < hi ? (hi - 1) / I - lo / I + 1 : 0);
       }
+
       if (cta == 0 && a.rec_ids) {
 #pragma unroll 1
         for (int p = rtid; p < T * K; p += NT) {
@@ -877,6 +892,40 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       if (!ctl->abort && !spin_geq(&a.counters[2], (uint32_t)G, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_PARTIAL);
       stamp(a, 11);
     }
+    // while thread 0 waits for every CTA: per token, the list of partial-sum slots that hold it
+#pragma unroll 1
+      for (int t = cw - 1; cw > 0 && t < T; t += NCW - 1) {
+        int n = 0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < G; c0 += 32) {
+          const int c = c0 + lane;
+          uint32_t cnt = 0, sl[2] = {0u, 0u};
+          if (c < G) {
+            const int a0 = ctl->tab_a0[c], ns = min((int)ctl->tab_n[c], 2);
+#pragma unroll
+            for (int sg = 0; sg < 2; ++sg) {
+              if (sg < ns) {
+                const uint32_t msk = ctl->act_mask[a0 + sg];
+                if ((msk >> t) & 1u) {
+                  sl[cnt] = ((uint32_t)c * DEC_MAXSEG + sg) * T + __popc(msk & ((1u << t) - 1u));
+                  ++cnt;
+                }
+              }
+            }
+          }
+          uint32_t incl = cnt;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += v;
+          }
+          const int pos = n + (int)(incl - cnt);
+          if (cnt > 0) ctl->slot[t][pos] = (uint16_t)sl[0];
+          if (cnt > 1) ctl->slot[t][pos + 1] = (uint16_t)sl[1];
+          n += (int)__shfl_sync(FULL, incl, 31);
+        }
+        if (lane == 0) ctl->nslot[t] = n;
+      }
     named_bar(BAR_C, CT);
     if (!ctl->abort) {
       const int nr = r1 - r0;
@@ -884,23 +933,16 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       for (int pi = cw; pi < T * nr; pi += NCW) {
         const int t = pi / nr, rr = pi % nr, row = r0 + rr;
         // every partial this lane needs is loaded before any is added (independent L2 reads in flight)
-        float v[DEC_MAXGRID / 32][2];
+        const int ns = ctl->nslot[t];
+        float v[2 * DEC_MAXGRID / 32];
 #pragma unroll
-        for (int k = 0; k < DEC_MAXGRID / 32; ++k) {
-          const int c = lane + 32 * k;
-          const int a0 = c < G ? ctl->tab_a0[c] : 0, ns = c < G ? ctl->tab_n[c] : 0;
-#pragma unroll
-          for (int sg = 0; sg < 2; ++sg) {
-            const uint32_t msk = sg < ns ? ctl->act_mask[a0 + sg] : 0u;
-            const bool use = (msk >> t) & 1u;
-            const int tl = __popc(msk & ((1u << t) - 1u));
-            const size_t slot = ((size_t)c * DEC_MAXSEG + sg) * T + tl;
-            v[k][sg] = use ? __ldcg(a.partial + slot * H + row) : 0.f;
-          }
+        for (int k = 0; k < 2 * DEC_MAXGRID / 32; ++k) {
+          const int q = lane + 32 * k;
+          v[k] = q < ns ? __ldcg(a.partial + (size_t)ctl->slot[t][q] * H + row) : 0.f;
         }
         float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < DEC_MAXGRID / 32; ++k) acc += v[k][0] + v[k][1];
+        for (int k = 0; k < 2 * DEC_MAXGRID / 32; ++k) acc += v[k];
         // rare: a CTA whose unit range touches more than two experts
 #pragma unroll 1
         for (int c = lane; c < G; c += 32) {

@@ -11,7 +11,7 @@ constexpr int DEC_THREADS = (DEC_NCW + 1) * 32;   // + one producer warp
 constexpr int DEC_TMAX = 16;                      // largest T of the fused decode kernel
 constexpr int DEC_MAXSEG = 4;                     // expert segments one CTA's unit range may touch
 constexpr int DEC_MAXNS = 24;                     // ring stages
-constexpr int DEC_MAXGRID = 256;                  // CTAs (one per SM)
+constexpr int DEC_MAXGRID = 160;                  // CTAs (one per SM)
 
 // device error bits
 enum : uint32_t {
