@@ -118,8 +118,9 @@ MOE_API const char *moe_last_cuda_error(void);
  * 4 shared gate [Is][H], 5 shared up [Is][H], 6 shared down [H][Is]; index = expert for 1..3. */
 MOE_API int moe_block_debug_dequant(moe_block_t *blk, int which, int index, float *out_device, void *stream);
 
-/* Routing of the last forward call, copied to device buffers (any may be NULL): logits [T][E+1] fp32,
- * ids [T][k] int32 ascending, weights [T][k] fp32 aligned with ids, sigmoid gate [T] fp32. */
+/* Routing of the last forward call, copied to device buffers (any may be NULL): ids [T][k] int32 ascending,
+ * weights [T][k] fp32 aligned with ids, sigmoid gate [T] fp32 for its first T tokens; logits [T][E+1] fp32 only
+ * for calls with T <= 16 (must be NULL otherwise). */
 MOE_API int moe_block_debug_last_routing(moe_block_t *blk, int T, float *logits, int32_t *ids, float *weights,
                                  float *sgate, void *stream);
 

@@ -1,10 +1,11 @@
 """CUDA path vs the float64 oracle, through the C ABI (ctypes). Dequantised weights and expert ids must match
-bit for bit; outputs within max|err| <= 2e-3 * RMS(out_oracle) (fp16 output, fp32 accumulation)."""
+bit for bit; outputs within 2e-3 * RMS(out_oracle) beyond the fp16 output's own rounding (fp16 output, fp32
+accumulation; see tests._cases.check_tol)."""
 import numpy as np
 import pytest
 
 import oracle.moe_oracle as O
-from tests._cases import make_case, rel_err, structural
+from tests._cases import check_tol, make_case, rel_err, structural
 from w4a16_top_mixture_gb300 import build, lib, synth
 
 pytestmark = pytest.mark.gpu
@@ -83,8 +84,8 @@ def test_tiny_t1(seed):
     blk = make_block(cfg, w)
     out, _, _ = run(blk, x)
     check_routing(blk, r, 1, cfg.top_k)
-    e = rel_err(out, r["out"])
-    assert e <= TOL, e
+    ok, e, plain = check_tol(out, r["out"])
+    assert ok, (e, plain)
     cos, ratio, moved = structural(out, r)
     assert cos >= 0.999 and abs(ratio - 1) <= 0.02 and moved >= 0.5
     blk.close()
@@ -123,9 +124,9 @@ def test_prod_t1(prod_block, seed):
     r = O.block_forward(w, x, cfg.top_k)
     out, _, _ = run(blk, x)
     check_routing(blk, r, 1, cfg.top_k)
-    e = rel_err(out, r["out"])
-    print(f"prod T=1 seed {seed}: max|err|/RMS = {e:.3e}")
-    assert e <= TOL, e
+    ok, e, plain = check_tol(out, r["out"])
+    print(f"prod T=1 seed {seed}: err beyond fp16 rounding/RMS = {e:.3e} (plain {plain:.3e})")
+    assert ok, (e, plain)
     cos, ratio, moved = structural(out, r)
     assert cos >= 0.999 and abs(ratio - 1) <= 0.02 and moved >= 0.5
 
@@ -137,9 +138,9 @@ def test_prod_ragged_batches(prod_block, T):
     r = O.block_forward(w, x, cfg.top_k)
     out, _, _ = run(blk, x)
     check_routing(blk, r, T, cfg.top_k)
-    e = rel_err(out, r["out"])
-    print(f"prod T={T}: max|err|/RMS = {e:.3e}")
-    assert e <= TOL, e
+    ok, e, plain = check_tol(out, r["out"])
+    print(f"prod T={T}: err beyond fp16 rounding/RMS = {e:.3e} (plain {plain:.3e})")
+    assert ok, (e, plain)
 
 
 def test_prod_t16_zipf():
@@ -150,10 +151,10 @@ def test_prod_t16_zipf():
     blk = make_block(cfg, w)
     out, _, _ = run(blk, x)
     check_routing(blk, r, 16, cfg.top_k)
-    e = rel_err(out, r["out"])
-    print(f"zipf T=16: {U} unique experts, max|err|/RMS = {e:.3e}")
+    ok, e, plain = check_tol(out, r["out"])
+    print(f"zipf T=16: {U} unique experts, err beyond fp16 rounding/RMS = {e:.3e} (plain {plain:.3e})")
     assert U < 16 * cfg.top_k      # reuse across tokens
-    assert e <= TOL, e
+    assert ok, (e, plain)
     blk.close()
 
 
@@ -180,7 +181,7 @@ def test_batched_equals_token_by_token(prod_block):
     batched, _, _ = run(blk, x)
     single = np.concatenate([run(blk, x[t:t + 1])[0] for t in range(16)], 0)
     r = O.block_forward(w, x, cfg.top_k)
-    assert rel_err(batched, r["out"]) <= TOL and rel_err(single, r["out"]) <= TOL
+    assert check_tol(batched, r["out"])[0] and check_tol(single, r["out"])[0]
     np.testing.assert_allclose(batched, single, rtol=0, atol=2 * TOL * np.sqrt(np.mean(r["out"] ** 2)))
 
 
@@ -224,5 +225,5 @@ def test_bounded_wait_reports_timeout_and_recovers():
     assert s == -5 and (flags & 1), (s, flags)
     blk.set_wait(0, False)
     out, _, _ = run(blk, x)
-    assert rel_err(out, r["out"]) <= TOL
+    assert check_tol(out, r["out"])[0]
     blk.close()

@@ -129,9 +129,9 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   if (e == cudaSuccess) e = cudaMalloc(&b->partial, decode_partial_floats(L, b->num_sms, T) * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->counters, 8 * 4);
   if (e == cudaSuccess) e = cudaMemset(b->counters, 0, 8 * 4);
-  if (e == cudaSuccess) e = cudaMalloc(&b->rec_ids, (size_t)T * c.top_k * 4);
-  if (e == cudaSuccess) e = cudaMalloc(&b->rec_w, (size_t)T * c.top_k * 4);
-  if (e == cudaSuccess) e = cudaMalloc(&b->rec_sg, (size_t)T * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->rec_ids, (size_t)c.max_tokens * c.top_k * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->rec_w, (size_t)c.max_tokens * c.top_k * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->rec_sg, (size_t)c.max_tokens * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->xbuf, (size_t)c.max_tokens * c.hidden * 2);
   if (e == cudaSuccess) e = cudaMalloc(&b->obuf, (size_t)c.max_tokens * c.hidden * 2);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -225,7 +225,9 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
     a.T = n;
     a.logits = b->logits; a.hs = b->hs; a.partial = b->partial;
     a.counters = b->counters; a.status = b->status;
-    a.rec_ids = b->rec_ids; a.rec_w = b->rec_w; a.rec_sg = b->rec_sg;
+    a.rec_ids = b->rec_ids + (size_t)t0 * b->cfg.top_k;
+    a.rec_w = b->rec_w + (size_t)t0 * b->cfg.top_k;
+    a.rec_sg = b->rec_sg + t0;
     a.timeout_ns = b->timeout_ns;
     a.skip_arrive = b->skip_arrive;
     a.trace = b->trace;
@@ -301,7 +303,8 @@ extern "C" int moe_block_debug_dequant(moe_block_t* b, int which, int index, flo
 
 extern "C" int moe_block_debug_last_routing(moe_block_t* b, int T, float* logits, int32_t* ids, float* w,
                                             float* sg, void* stream) {
-  if (!b || T < 1 || T > b->dec_T || T > b->last_T) return MOE_ERR_INVALID_ARG;
+  if (!b || T < 1 || T > b->last_T) return MOE_ERR_INVALID_ARG;
+  if (logits && T > b->dec_T) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   const int E = b->cfg.n_experts, K = b->cfg.top_k;
   if (logits) CK(cudaMemcpyAsync(logits, b->logits, (size_t)T * (E + 1) * 4, cudaMemcpyDeviceToDevice, st));

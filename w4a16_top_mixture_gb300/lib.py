@@ -201,7 +201,7 @@ class MoeBlock:
     def last_routing(self, T, stream=None):
         import torch
         E, K = self.cfg.n_experts, self.cfg.top_k
-        lg = torch.empty((T, E + 1), dtype=torch.float32, device="cuda")
+        lg = torch.empty((T, E + 1), dtype=torch.float32, device="cuda") if T <= 16 else None
         ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
         w = torch.empty((T, K), dtype=torch.float32, device="cuda")
         sg = torch.empty((T,), dtype=torch.float32, device="cuda")
