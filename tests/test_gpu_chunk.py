@@ -13,13 +13,12 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 TOL = 2e-3
 
 
-@pytest.mark.parametrize("routing", ["uniform", "zipf"])
-def test_chunk_512(routing):
+@pytest.mark.parametrize("T,routing", [(40, "uniform"), (512, "uniform"), (512, "zipf")])
+def test_chunk(T, routing):
     import torch
     build.build()
     cfg = synth.PROD
-    T = 512
-    w, x = make_case(cfg, T, 41 if routing == "uniform" else 42, routing=routing)
+    w, x = make_case(cfg, T, 41 + T if routing == "uniform" else 42, routing=routing)
     r = O.block_forward(w, x, cfg.top_k)
     counts = np.bincount(r["ids"].ravel(), minlength=cfg.n_experts)
     blk = lib.MoeBlock.from_config(cfg, max_tokens=T)
@@ -35,10 +34,11 @@ def test_chunk_512(routing):
     np.testing.assert_allclose(rt["w"].cpu().numpy(), r["w"], rtol=0, atol=2e-5)
     ok, e, plain = check_tol(got, r["out"])
     cos, ratio, moved = structural(got, r)
-    print(f"T=512 {routing}: largest expert group {counts.max()}, experts used {np.count_nonzero(counts)}, "
+    print(f"T={T} {routing}: largest expert group {counts.max()}, experts used {np.count_nonzero(counts)}, "
           f"err beyond fp16 rounding/RMS = {e:.3e} (plain {plain:.3e}), cos {cos:.6f}")
     assert ok, (e, plain)
     assert cos >= 0.999 and abs(ratio - 1) <= 0.02 and moved >= 0.5
+    assert blk.last_launch_count() == 8          # the tensor-core chunk path, not the decode loop
     if routing == "zipf":
         assert counts.max() >= 64          # a head expert reaches a dense-tile-sized group
     blk.close()

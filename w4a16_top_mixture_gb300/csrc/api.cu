@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include "../../include/moe_block.h"
+#include "chunk.cuh"
 #include "decode.cuh"
 #include "layout.cuh"
 #include "repack.cuh"
@@ -33,6 +34,12 @@ struct moe_block {
   int last_T = 0;
   DecodeLaunch plans[DEC_TMAX + 1];                // launch plan per T, computed at create
   uint64_t* trace = nullptr;                       // optional phase-timestamp buffer (debug)
+  // prompt-chunk path (T > 16): GEMM-layout weight copy and its scratch, only when max_tokens > 16
+  bool chunk = false;
+  uint8_t* gstore = nullptr;
+  uint8_t* cscratch = nullptr;
+  GemmLayout G;
+  ChunkScratch CS;
 };
 
 static thread_local char g_cuda_err[256] = "";
@@ -76,6 +83,8 @@ static void free_all(moe_block* b) {
   cudaFree(b->rec_sg);
   cudaFree(b->xbuf);
   cudaFree(b->obuf);
+  cudaFree(b->gstore);
+  cudaFree(b->cscratch);
 }
 
 extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out) {
@@ -134,6 +143,15 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   if (e == cudaSuccess) e = cudaMalloc(&b->rec_sg, (size_t)c.max_tokens * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->xbuf, (size_t)c.max_tokens * c.hidden * 2);
   if (e == cudaSuccess) e = cudaMalloc(&b->obuf, (size_t)c.max_tokens * c.hidden * 2);
+  if (e == cudaSuccess && c.max_tokens > DEC_TMAX) {
+    b->chunk = true;
+    e = cudaMalloc(&b->gstore, gemm_store_bytes(L));
+    if (e == cudaSuccess) e = cudaMalloc(&b->cscratch, chunk_scratch_bytes(L, c.max_tokens));
+    if (e == cudaSuccess) {
+      b->G = gemm_layout_carve(L, b->gstore);
+      b->CS = chunk_scratch_carve(L, c.max_tokens, b->cscratch);
+    }
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_all(b);
@@ -197,6 +215,7 @@ extern "C" int moe_block_load_weights(moe_block_t* b, const moe_block_weights_t*
   src.sh_down_q = (const uint8_t*)dptr[18]; src.sh_down_s = (const uint16_t*)dptr[19]; src.sh_down_b = (const uint16_t*)dptr[20];
   RepackDst dst{b->router, b->sh_gu, b->sh_dn, b->ex_gu, b->ex_dn};
   cudaError_t e = repack_all(src, b->L, dst, st);
+  if (e == cudaSuccess && b->chunk) e = gemm_repack(src, b->G, st);
   if (e == cudaSuccess && w->rms_gamma) {
     e = cudaMemcpyAsync(b->gamma, w->rms_gamma, H * 2, on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
                         st);
@@ -213,6 +232,14 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
                        cudaStream_t st) {
   b->last_launches = 0;
   b->last_T = T;
+  if (T > DEC_TMAX && b->chunk) {
+    int n = 0;
+    cudaError_t e = chunk_forward(b->L, b->G, b->CS, b->num_sms, x, out, T, gamma, eps, b->rec_ids, b->rec_w,
+                                  b->rec_sg, b->status, b->timeout_ns, st, &n);
+    b->last_launches = n;
+    if (e != cudaSuccess) return cuda_fail(e, "chunk forward");
+    return MOE_OK;
+  }
   for (int t0 = 0; t0 < T; t0 += DEC_TMAX) {
     const int n = T - t0 < DEC_TMAX ? T - t0 : DEC_TMAX;
     const DecodeLaunch& pl = b->plans[n];
