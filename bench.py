@@ -34,6 +34,34 @@ WORKLOAD = ("decode T=1: hidden 2048, 256 experts top-8 renormalised, expert int
 SEED = 1
 
 
+def rank_env():
+    """(world size, rank, local rank) from the torchrun environment; 1 / 0 / 0 without it."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(rank):
+    """Each replica draws its own weights and tokens."""
+    return SEED + 1000 * rank
+
+
+def max_over_ranks(v):
+    """Largest value of v over the process group (v itself without one): the slowest rank sets the time."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(v)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, steps, elapsed_ms):
+    """Tokens per second of the whole job: every rank processes `steps` tokens in at most `elapsed_ms`."""
+    return world * steps / (elapsed_ms * 1e-3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -56,9 +84,8 @@ def traffic_record():
 def kernel_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a16_top_mixture_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ("decode.cu", "decode.cuh", "layout.cuh", "ptx.cuh"):   # the sources k_decode is built from
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
 
@@ -138,8 +165,7 @@ print(json.dumps({{"tokens": n, "seconds": el}}))
 
 def run_reference(args):
     """Reference arm: the float64 oracle on the host cores, same metric/unit; each step = one token."""
-    import torch.distributed as dist  # noqa: F401
-    rank = int(os.environ.get("RANK", "0"))
+    _, rank, _ = rank_env()
     if rank != 0:
         return
     budget = float(os.environ.get("MOE_REF_BUDGET_S", "90"))
@@ -178,9 +204,7 @@ def run_ours(args):
 
     from w4a16_top_mixture_gb300 import build, lib
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
@@ -190,7 +214,7 @@ def run_ours(args):
     NL = args.layers
     blocks = []
     for l in range(NL):
-        w = synth.gen_layer(cfg, SEED + 1000 * rank, l)
+        w = synth.gen_layer(cfg, rank_seed(rank), l)
         b = lib.MoeBlock.from_config(cfg, max_tokens=1)
         b.load_weights(w)                      # host arrays: copied and repacked by the library
         blocks.append(b)
@@ -251,10 +275,7 @@ def run_ours(args):
         s, f = b.status()
         if s != 0:
             raise RuntimeError(f"device status {s} flags {f:#x}")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms)
 
     # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
     Ke = min(K, 2000)
@@ -267,10 +288,7 @@ def run_ours(args):
     for i in range(Ke):
         blocks[i % NL].forward_host(xpin[i:i + 1], opin[i:i + 1], stream=st)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s)
 
     if rank == 0:
         bytes_call = synth.unique_weight_bytes(cfg, cfg.top_k)
@@ -278,7 +296,7 @@ def run_ours(args):
         achieved = bytes_call / (kern_ms * 1e-3) / 1e9
         tr = traffic_record()
         cpu_v, cpu_d = cpu_baseline() if not args.skip_cpu else (None, {"tokens": 0, "seconds": 0.0})
-        value = world * K / (elapsed_ms * 1e-3)
+        value = whole_job_value(world, K, elapsed_ms)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
@@ -296,7 +314,7 @@ def run_ours(args):
             "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{cpu_d['tokens']} T=1 tokens through one production block in "
                                        f"{cpu_d['seconds']:.1f} s, single-threaded float64 numpy"},
-            "e2e": {"value": world * Ke / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 2 * cfg.hidden,
+            "e2e": {"value": whole_job_value(world, Ke, e2e_s * 1e3), "unit": "tokens/s", "h2d_bytes_per_step": 2 * cfg.hidden,
                     "d2h_bytes_per_step": 2 * cfg.hidden,
                     "how": "moe_block_forward_host: pinned x -> device, forward, out -> host, stream sync, per step"},
             "gpu_launches": launches,
