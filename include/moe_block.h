@@ -131,8 +131,11 @@ MOE_API int moe_block_debug_last_routing(moe_block_t *blk, int T, float *logits,
 MOE_API int moe_block_debug_set_wait(moe_block_t *blk, uint32_t timeout_us, int skip_arrive);
 
 /* Phase timestamps for performance analysis: when trace_device is non-NULL, every later decode call writes
- * %globaltimer nanosecond stamps at its phase boundaries into trace_device[cta * 32 + slot] (uint64, device
- * memory of at least 32 * number-of-SMs entries, caller-owned); NULL switches tracing off. */
+ * SM clock stamps (clock64) at its phase boundaries into trace_device[cta * 32 + slot], %globaltimer
+ * nanoseconds at the CTA's start and end into slots 30 and 31 (to place every CTA on one time axis), and
+ * per-warp clock stamps into trace_device[32 * G + (cta * 16 + warp) * 4 + k] (G = number of SMs). A slot a
+ * call does not reach holds 0. trace_device is uint64 device memory of at least 96 * number-of-SMs entries,
+ * caller-owned; NULL switches tracing off. */
 MOE_API int moe_block_debug_set_trace(moe_block_t *blk, void *trace_device);
 
 /* ---- allocation-free routing ----

@@ -23,7 +23,7 @@ struct moe_block {
   uint16_t* gamma = nullptr;
   bool loaded = false, has_gamma = false;
   int dec_T = 0;                                   // largest T the decode scratch holds
-  float *logits = nullptr, *hs = nullptr, *partial = nullptr;
+  float *logits = nullptr, *hs = nullptr, *hbuf = nullptr;
   uint32_t *counters = nullptr, *status = nullptr;
   int32_t* rec_ids = nullptr;
   float *rec_w = nullptr, *rec_sg = nullptr;
@@ -76,7 +76,7 @@ static void free_all(moe_block* b) {
   cudaFree(b->gamma);
   cudaFree(b->logits);
   cudaFree(b->hs);
-  cudaFree(b->partial);
+  cudaFree(b->hbuf);
   cudaFree(b->counters);
   cudaFree(b->rec_ids);
   cudaFree(b->rec_w);
@@ -135,7 +135,7 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   if (e == cudaSuccess) e = cudaMalloc(&b->gamma, (size_t)c.hidden * 2);
   if (e == cudaSuccess) e = cudaMalloc(&b->logits, (size_t)T * (c.n_experts + 1) * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->hs, (size_t)T * c.shared_inter * 4);
-  if (e == cudaSuccess) e = cudaMalloc(&b->partial, decode_partial_floats(L, b->num_sms, T) * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->hbuf, decode_hbuf_floats(L, T) * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->counters, 8 * 4);
   if (e == cudaSuccess) e = cudaMemset(b->counters, 0, 8 * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->rec_ids, (size_t)c.max_tokens * c.top_k * 4);
@@ -250,7 +250,7 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
     a.gamma = gamma;
     a.eps = eps;
     a.T = n;
-    a.logits = b->logits; a.hs = b->hs; a.partial = b->partial;
+    a.logits = b->logits; a.hs = b->hs; a.hbuf = b->hbuf;
     a.counters = b->counters; a.status = b->status;
     a.rec_ids = b->rec_ids + (size_t)t0 * b->cfg.top_k;
     a.rec_w = b->rec_w + (size_t)t0 * b->cfg.top_k;

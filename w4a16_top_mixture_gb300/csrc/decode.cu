@@ -1,19 +1,22 @@
-// Fused decode kernel of the W4A16 routed-MoE block (T <= 16 tokens): one cooperative, persistent launch with
+// Fused decode kernel of the W4A16 routed-MoE block (T <= 16 tokens): one persistent launch with
 // one CTA per SM.
 //
 // Roles inside a CTA: warp 0 is the producer (one lane issues 1-D bulk copies of contiguous weight ranges
 // into a ring of shared-memory stages, each guarded by a "full" and an "empty" mbarrier); warps 1..16 are
 // consumers. Work a CTA owns, in stream order:
-//   A1  its share of the router rows (int8)           -> logits to global, then a grid-wide arrival count
+//   A1  its share of the router rows (int8)            -> logits to global, then a grid-wide arrival count
 //   R   routing: every CTA waits for all logits and computes softmax -> top-k -> renormalise for every token
-//       itself (identical arithmetic everywhere), then buckets tokens by expert
-//   A2  its share of the shared-expert gate/up units   -> hs = silu(g)*u to global, arrival count
-//   B   its share of the routed units: all (active expert, intermediate unit) pairs split evenly across the
-//       grid. For each unit: h = silu(Wg x)*(Wu x) per routed token, then that unit's column of the down
-//       matrix times h, accumulated per output row into a weighted partial sum per (segment, token)
-//   C   its share of the shared-down output rows (needs all hs: waits on the hs arrival count)
-//   D   after a grid-wide count of finished partials: for its output rows, out = sum of the partials in a
-//       fixed order + sigmoid(g) * shared row (+ residual), rounded to fp16 once
+//       itself (identical arithmetic everywhere), buckets the (token, expert) pairs by expert and plans its
+//       share of the routed units; the producer is released as soon as the plan exists
+//   A2  (concurrently with R) its share of the shared-expert gate/up units -> hs to global, arrival count
+//   B1  its share of all (active expert, intermediate unit) pairs: h = silu(Wg x) * (Wu x) for every token of
+//       the expert, written to a global row per (expert, token) pair; arrival count
+//   C   the shared expert's down projection for the CTA's own output rows (needs every CTA's hs)
+//   B2  after every CTA's h is in: the routed down projection for the CTA's own output rows, every active
+//       expert's rows of the down matrix against the staged h of its pairs
+//   D   out = sum over the token's experts, in a fixed order, of w * y + sigmoid(g) * shared (+ residual),
+//       rounded to fp16 once
+// The output rows a CTA owns are its own from C to D, so no cross-CTA reduction follows the down projection.
 // Every grid-wide or mbarrier wait is bounded by a timeout; a timeout records an error bit and the CTA
 // drains its in-flight copies and leaves, so no wait can hang the GPU.
 #include <cuda_fp16.h>
@@ -32,6 +35,7 @@ constexpr int BAR_C = 1;       // named barrier of all consumer warps
 constexpr int BAR_A = 2;       // the shared-expert team
 constexpr int BAR_R = 3;       // the routing team
 constexpr uint32_t FULL = 0xFFFFFFFFu;
+constexpr int PMAX = DEC_TMAX * 16;   // (token, expert) pairs
 
 constexpr size_t c_align16(size_t v) { return (v + 15) & ~(size_t)15; }
 
@@ -46,11 +50,9 @@ struct Shape {
   static constexpr size_t SU = c_align16(2 * (size_t)H + 2 * (size_t)GB * 4);
   static constexpr size_t SDR = c_align16((size_t)Is + (size_t)GS * 4);
   static constexpr size_t EU = c_align16((size_t)H + 2 * (size_t)GB * 4);
-  static constexpr size_t DSB = (size_t)H * 4;
-  static constexpr size_t DCB = (size_t)H / 2;
-  static constexpr size_t DB = DSB + 64 * DCB;
+  static constexpr size_t DR = c_align16((size_t)I / 2 + (size_t)GI * 4);
   static constexpr size_t exgu_expert = (size_t)I * EU;
-  static constexpr size_t exdn_expert = (size_t)GI * DB;
+  static constexpr size_t exdn_expert = (size_t)H * DR;
 };
 using ShapeProd = Shape<2048, 256, 8, 512, 512>;
 using ShapeTiny = Shape<512, 32, 4, 128, 128>;
@@ -59,50 +61,53 @@ struct Ctl {
   uint64_t full[DEC_MAXNS];
   uint64_t empty[DEC_MAXNS];
   uint64_t route_ready;
+  uint64_t hbar;                      // the routed h of a single-token launch has landed in shared memory
   volatile int abort;
-  int U;
-  int nseg;
-  int issued;
-  int seg_a[DEC_MAXSEG], seg_e[DEC_MAXSEG], seg_u0[DEC_MAXSEG], seg_u1[DEC_MAXSEG], seg_n[DEC_MAXSEG];
-  uint8_t seg_tok[DEC_MAXSEG][DEC_TMAX];
-  float seg_w[DEC_MAXSEG][DEC_TMAX];
+  int U;                              // active experts
+  int nseg;                           // segments of this CTA's routed-unit range
+  int seg_a[DEC_MAXSEG], seg_u0[DEC_MAXSEG], seg_u1[DEC_MAXSEG];
   int ids[DEC_TMAX][16];
   float wts[DEC_TMAX][16];
   float sg[DEC_TMAX];
   float rn[DEC_TMAX];
-  uint32_t emask[512];
-  uint16_t act_e[512];
+  uint32_t emask[512];                // tokens routed to each expert
+  uint16_t act_e[512];                // active experts, in bucket order
   uint32_t act_mask[512];
-  int warp_tot[NCW];
-  uint16_t tab_a0[DEC_MAXGRID];   // per CTA: first active-expert index of its unit range
-  uint8_t tab_n[DEC_MAXGRID];     // per CTA: number of segments
-  int nslot[DEC_TMAX];            // per token: number of partial-sum slots holding it
-  uint16_t slot[DEC_TMAX][2 * DEC_MAXGRID];   // per token: the slots, in (CTA, segment) order
+  uint16_t act_pb[513];               // first sorted pair of each active expert (act_pb[U] = number of pairs)
+  uint8_t pair_tok[PMAX];             // token of each sorted pair
+  float pair_w[PMAX];                 // routing weight of each sorted pair
+  uint8_t tok_pair[DEC_TMAX][16];     // token t's j-th expert -> its sorted pair
+  int warp_tot[NCW], warp_tot2[NCW];
+  unsigned long long tclk[32];        // phase stamps (SM clock), flushed to the trace buffer at exit
+  unsigned long long wclk[NCW][4];    // per-warp stamps
 };
 constexpr int CTL_BYTES = (sizeof(Ctl) + 127) & ~127;
 
 struct Smem {   // byte offsets of the dynamic shared-memory regions
-  int xh, xs, hss, hseg, shs, ring;
+  int xh, xs, hss, hst, hsm, yv, shs, ring;
 };
 
 // xh: x as fp16 [T][P][4 blocks][LW lanes] uint4 (the 8 columns of a block in pair order 0 4 1 5 2 6 3 7);
 // xs: per (token, 32-column chunk) the sums of x over the chunk's "low" and "high" pair columns;
-// hseg: phase B's h, and before phase B the shared expert's hs [T][Is]; hss: 16-column sums of hs;
-// shs: this CTA's shared-down rows; ring: the weight stages.
+// hss: 16-column sums of the shared expert's hs; hst: phase C's hs [T][Is], then phase B2's staged routed h
+// (hp vectors of I floats, each in the lane order of the down dot); hsm: 16-column sums of the staged h;
+// yv: routed down results [pair][row]; shs: shared down results [token][row]; ring: the weight stages.
 template <class LT>
-__host__ __device__ inline Smem smem_map(const LT& L, int T, int grid, int hseg_floats) {
+__host__ __device__ inline Smem smem_map(const LT& L, int T, int grid, int hp) {
   Smem m;
+  const int rows = (L.H + grid - 1) / grid;
   int o = CTL_BYTES;
   m.xh = o;   o += (T * L.H * 2 + 127) & ~127;
   m.xs = o;   o += (T * L.NCH * 8 + 127) & ~127;
   m.hss = o;  o += (T * (L.Is / 16) * 4 + 127) & ~127;
-  m.hseg = o;
+  m.hst = o;
   {
-    int hx = hseg_floats > T * L.Is ? hseg_floats : T * L.Is;
-    o += (hx * 4 + 127) & ~127;
+    const int f = hp * L.I > T * L.Is ? hp * L.I : T * L.Is;
+    o += (f * 4 + 127) & ~127;
   }
-  int rpc = (L.H + grid - 1) / grid;
-  m.shs = o;  o += (T * rpc * 4 + 127) & ~127;
+  m.hsm = o;  o += (hp * (L.I / 16) * 4 + 127) & ~127;
+  m.yv = o;   o += (T * L.K * rows * 4 + 127) & ~127;
+  m.shs = o;  o += (T * rows * 4 + 127) & ~127;
   m.ring = o;
   return m;
 }
@@ -115,14 +120,11 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-
-__device__ __forceinline__ void stamp(const DecodeArgs& a, int slot) {
-  if (a.trace) a.trace[blockIdx.x * 32 + slot] = globaltimer();
-}
-// per-warp stamps (lane 0): trace[grid*32 + (cta*16 + warp)*4 + k]
-__device__ __forceinline__ void wstamp(const DecodeArgs& a, int cw, int k) {
-  if (a.trace && (threadIdx.x & 31) == 0) a.trace[gridDim.x * 32 + (blockIdx.x * 16 + cw) * 4 + k] = globaltimer();
-}
+// Phase stamps read the SM clock into shared memory (a few cycles, so tracing barely perturbs the kernel) and
+// are written out once at exit: trace[cta*32 + slot] (slots 30 / 31: globaltimer at start / end, which place
+// the CTA's clock on a common time axis) and per-warp stamps trace[grid*32 + (cta*16 + warp)*4 + k].
+#define stamp(a, slot) do { if ((a).trace) ctl->tclk[(slot)] = clock64(); } while (0)
+#define wstamp(a, cw, k) do { if ((a).trace && (threadIdx.x & 31) == 0) ctl->wclk[(cw)][(k)] = clock64(); } while (0)
 
 __device__ __forceinline__ void set_error(const DecodeArgs& a, Ctl* ctl, uint32_t bit) {
   atomicOr(a.status, bit);
@@ -133,6 +135,14 @@ template <int NR, int TK>
 struct DotR {
   float v[TK][NR];
 };
+
+// Routed h vectors are stored in the lane order of the down dot: unit u = 16 c + 4 j + m (lane chunk c,
+// float4 j, component m) sits at float index (j * (I/16) + c) * 4 + m, so that a linear copy of a vector into
+// shared memory lets lane c read its float4 j at consecutive 16-byte addresses across the warp.
+template <int I>
+__device__ __forceinline__ int hpos(int u) {
+  return (((u & 15) >> 2) * (I / 16) + (u >> 4)) * 4 + (u & 3);
+}
 
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
@@ -229,17 +239,61 @@ __device__ __noinline__ DotR<NR, TK> dot_rows(const uint8_t* r0, const uint8_t* 
   return out;
 }
 
+// Routed down projection of one output row against the staged h of up to NP pairs (all tokens of one expert
+// in a batch). The row is I int4 codes in canonical packing followed by I/64 (s, b) pairs; lane l covers the
+// 16-column chunks c = l + 32 m. The staged h of a pair is stored as float4 [4][I/16] (element (j, c) holds
+// columns 16c + 4j .. 16c + 4j + 3), so the lanes of a warp read consecutive 16 bytes; hsm holds the 16-column
+// sums of h. Codes are unpacked once and reused for every pair: y[p] = sum_g s_g * sum(q h) + b_g * sum(h),
+// warp-reduced (every lane receives every y[p]).
+template <int I, int NP>
+__device__ __forceinline__ void dot_down(const uint8_t* __restrict__ row, const float4* __restrict__ hst,
+                                         const float* __restrict__ hsm, int p0, int np, float (&y)[NP]) {
+  constexpr int NC = I / 16;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) y[q] = 0.f;
+#pragma unroll
+  for (int c0 = 0; c0 < NC; c0 += 32) {
+    const int c = c0 + lane;
+    if (NC % 32 == 0 || c < NC) {
+      const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+      float2 q[8];
+      unpack_int4_quad(w.x & 0xFFFFu, q[0], q[1]);
+      unpack_int4_quad(w.x >> 16, q[2], q[3]);
+      unpack_int4_quad(w.y & 0xFFFFu, q[4], q[5]);
+      unpack_int4_quad(w.y >> 16, q[6], q[7]);
+      const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + I / 2 + (c >> 2) * 4));
+#pragma unroll
+      for (int pp = 0; pp < NP; ++pp) {
+        if (pp < np) {
+          const float4* hv = hst + (size_t)(p0 + pp) * (4 * NC) + c;
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 h4 = hv[j * NC];
+            acc = __ffma2_rn(q[2 * j], make_float2(h4.x, h4.y), acc);
+            acc = __ffma2_rn(q[2 * j + 1], make_float2(h4.z, h4.w), acc);
+          }
+          y[pp] += sb.x * (acc.x + acc.y) + sb.y * hsm[(p0 + pp) * NC + c];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int pp = 0; pp < NP; ++pp) y[pp] = warp_sum(y[pp]);
+}
+
 // Top-k of one token's expert logits held by a warp. Lane l holds experts l*EPL .. l*EPL+EPL-1 (a lower lane
 // means lower indices) as order-preserving integer keys. Each of the k rounds takes the warp maximum of the lane
 // maxima (the lowest lane winning ties; within a lane the lowest index), and only the winning lane recomputes
 // its maximum. Lane j < k returns the j-th largest (index, logit).
-// Once the k experts are known, lane j asks L2 to prefetch this CTA's 1/G slice of the j-th one's weights
-// (pf_gu / pf_dn: the expert blocks, pf_gu_sz / pf_dn_sz bytes each): the grid as a whole starts pulling the
-// selected experts into L2 while the bucketing runs, ahead of the weight copies that follow it.
+// Once the k experts are known, lane j asks L2 to prefetch the weights of the j-th one that this CTA's share
+// of the work is likely to read: a 1/G slice of its gate/up block (the grid as a whole covers the expert) and
+// this CTA's own rows of its down matrix.
 template <int EPL>
 __device__ __noinline__ void warp_topk(const float* __restrict__ lg, int E, int K, int lane, int& my_idx,
                                        float& my_logit, const uint8_t* pf_gu, size_t pf_gu_sz,
-                                       const uint8_t* pf_dn, size_t pf_dn_sz) {
+                                       const uint8_t* pf_dn, size_t pf_dn_sz, size_t dn0, size_t dn1) {
   uint32_t key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
@@ -256,7 +310,6 @@ __device__ __noinline__ void warp_topk(const float* __restrict__ lg, int E, int 
   uint32_t my_key = 0;
   const int G = gridDim.x, c = blockIdx.x;
   const size_t gu0 = ((pf_gu_sz * c / G) & ~(size_t)15), gu1 = ((pf_gu_sz * (c + 1) / G) & ~(size_t)15);
-  const size_t dn0 = ((pf_dn_sz * c / G) & ~(size_t)15), dn1 = ((pf_dn_sz * (c + 1) / G) & ~(size_t)15);
 #pragma unroll 1
   for (int j = 0; j < K; ++j) {
     const uint32_t m = __reduce_max_sync(FULL, best);
@@ -274,7 +327,6 @@ __device__ __noinline__ void warp_topk(const float* __restrict__ lg, int E, int 
         if (key[i] > best) { best = key[i]; bi = i; }
     }
   }
-  // lane j < k starts the L2 prefetch of this CTA's slice of the j-th selected expert
   if (lane < K && pf_gu) {
     if (gu1 > gu0) prefetch_l2(pf_gu + (size_t)my_idx * pf_gu_sz + gu0, (uint32_t)(gu1 - gu0));
     if (dn1 > dn0) prefetch_l2(pf_dn + (size_t)my_idx * pf_dn_sz + dn0, (uint32_t)(dn1 - dn0));
@@ -284,21 +336,25 @@ __device__ __noinline__ void warp_topk(const float* __restrict__ lg, int E, int 
 }
 
 template <class SH, int TK>
-__global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS, int SS, int hseg_floats) {
+__global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS, int SS, int hp) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr SH L{};
   constexpr int H = SH::H, NCH = SH::NCH, LW = SH::LW, P = SH::P;
   constexpr int E = SH::E, K = SH::K, I = SH::I, Is = SH::Is;
+  constexpr int NC = I / 16;                 // 16-column chunks of a routed h vector
+  constexpr bool ONE = TK == 1;              // single-token launch (T == 1)
   const int G = gridDim.x, cta = blockIdx.x;
   const int T = a.T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem);
-  const Smem sm = smem_map(L, T, G, hseg_floats);
+  const Smem sm = smem_map(L, T, G, hp);
   uint4* xh = reinterpret_cast<uint4*>(smem + sm.xh);
   float2* xs = reinterpret_cast<float2*>(smem + sm.xs);
   float* hss = reinterpret_cast<float*>(smem + sm.hss);
-  float* hseg = reinterpret_cast<float*>(smem + sm.hseg);
-  float* hsn = hseg;   // shared-expert hs [T][Is], natural order, used before phase B
+  float* hst = reinterpret_cast<float*>(smem + sm.hst);
+  float4* hst4 = reinterpret_cast<float4*>(smem + sm.hst);
+  float* hsm = reinterpret_cast<float*>(smem + sm.hsm);
+  float* yv = reinterpret_cast<float*>(smem + sm.yv);
   float* shs = reinterpret_cast<float*>(smem + sm.shs);
   uint8_t* ring = smem + sm.ring;
 
@@ -306,11 +362,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
   const int ra = range_lo(E + 1, cta, G), rb = range_lo(E + 1, cta + 1, G);       // router rows
   const int sa = range_lo(Is, cta, G), sbn = range_lo(Is, cta + 1, G);           // shared units
   const int r0 = range_lo(H, cta, G), r1 = range_lo(H, cta + 1, G);             // output rows
+  const int nrow = r1 - r0;
   const int RPI = SS / (int)L.RR;                 // router rows per item
   const int SPI = (SS / (int)L.SU) & ~1;          // shared units per item (even)
   const int UPI = (SS / (int)L.EU) & ~1;          // expert units per item (even)
-  const int DPI = SS / (int)L.DCB;                // down columns per item
   const int SDPI = SS / (int)L.SDR;               // shared-down rows per item
+  const int DRPI = SS / (int)L.DR;                // routed-down rows per item
+  const int dn_items = (nrow + DRPI - 1) / DRPI;  // routed-down items per active expert
 
   if (threadIdx.x == 0) {
 #pragma unroll 1
@@ -319,12 +377,21 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       mbar_init(&ctl->empty[s], NCW);
     }
     mbar_init(&ctl->route_ready, 1);
+    mbar_init(&ctl->hbar, 1);
     ctl->abort = 0;
-    ctl->issued = 0;
+    if (a.trace) {
+      for (int i = 0; i < 32; ++i) ctl->tclk[i] = 0;
+      for (int i = 0; i < NCW * 4; ++i) ctl->wclk[i / 4][i % 4] = 0;
+      ctl->tclk[30] = globaltimer();
+    }
     fence_mbar_init();
   }
   __syncthreads();
   if (threadIdx.x == 0) stamp(a, 0);
+  // Programmatic dependent launch: the next kernel on the stream may be scheduled now (its CTAs take SMs as
+  // this grid's CTAs leave and run their setup and weight copies), and it waits for this whole grid before
+  // it touches global state.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -362,23 +429,21 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       if (ok && ctl->abort) ok = false;
       stamp(a, 17);
       const int nseg = ok ? ctl->nseg : 0;
+      const int U = ok ? ctl->U : 0;
 #pragma unroll 1
       for (int sgi = 0; ok && sgi < nseg; ++sgi) {
-        const int e = ctl->seg_e[sgi], u0 = ctl->seg_u0[sgi], u1 = ctl->seg_u1[sgi];
+        const int e = ctl->act_e[ctl->seg_a[sgi]], u0 = ctl->seg_u0[sgi], u1 = ctl->seg_u1[sgi];
         const uint8_t* gu = a.ex_gu + (size_t)e * L.exgu_expert;
 #pragma unroll 1
         for (int u = u0; ok && u < u1; u += UPI)
           ok = issue(gu + (size_t)u * L.EU, (uint32_t)(min(UPI, u1 - u) * L.EU));
-        const uint8_t* dn = a.ex_dn + (size_t)e * L.exdn_expert;
+      }
 #pragma unroll 1
-        for (int g = u0 / 64; ok && g * 64 < u1; ++g) {
-          const uint8_t* blk = dn + (size_t)g * L.DB;
-          ok = issue(blk, (uint32_t)L.DSB);
-          const int ga = max(u0, g * 64), gb = min(u1, g * 64 + 64);
+      for (int aa = 0; ok && aa < U; ++aa) {
+        const uint8_t* dn = a.ex_dn + (size_t)ctl->act_e[aa] * L.exdn_expert + (size_t)r0 * L.DR;
 #pragma unroll 1
-          for (int u = ga; ok && u < gb; u += DPI)
-            ok = issue(blk + L.DSB + (size_t)(u - g * 64) * L.DCB, (uint32_t)(min(DPI, gb - u) * L.DCB));
-        }
+        for (int rr = 0; ok && rr < nrow; rr += DRPI)
+          ok = issue(dn + (size_t)rr * L.DR, (uint32_t)(min(DRPI, nrow - rr) * L.DR));
       }
       stamp(a, 18);
       // drain: every issued copy must have landed before the CTA may leave
@@ -403,16 +468,24 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
     const int ctid = threadIdx.x - 32;
     int cs = 0;            // ring stage of the next item, mirrors the producer's order
     uint32_t cph = 0;      // its phase parity
-    auto acquire = [&]() -> const uint8_t* {
-      if (!ctl->abort && !mbar_wait(&ctl->full[cs], cph, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_FULL);
-      return ring + (size_t)cs * SS;
+    // the item i places after the next one (i = 0: the next one)
+    auto stage_at = [&](int i) -> const uint8_t* {
+      int s = cs + i;
+      uint32_t ph = cph;
+      while (s >= NS) { s -= NS; ph ^= 1u; }
+      if (!ctl->abort && !mbar_wait(&ctl->full[s], ph, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_FULL);
+      return ring + (size_t)s * SS;
     };
+    auto acquire = [&]() -> const uint8_t* { return stage_at(0); };
     auto release = [&]() {
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->empty[cs]);
       if (++cs == NS) { cs = 0; cph ^= 1u; }
     };
 
+    // Everything the consumers read or write in global memory (x, logits, counters, hs, h, out) may belong to
+    // the previous kernel on the stream until it has completed; the producer's weight copies above do not.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // ---- x prologue: (RMSNorm ->) fp16 activations in pair order, plus per-chunk pair-column sums; one
     // (token, 32-column chunk) item per consumer thread
     if (a.gamma) {
@@ -501,7 +574,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
     }
 
     // The warps split in two teams: RW routing warps wait for every CTA's logits and route, while the other AW
-    // warps compute this CTA's shared-expert gate/up units; both join again before the shared down rows.
+    // warps compute this CTA's shared-expert gate/up units; both join again before the routed gate/up.
     const int RW = T < 8 ? T : 8, AW = NCW - RW;
     if (cw < AW) {
       // ---- A2: shared-expert gate/up units, a pair per warp
@@ -552,17 +625,61 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
         set_error(a, ctl, ERR_WAIT_LOGITS);
       if (rtid == 0) stamp(a, 3);
       named_bar(BAR_R, NT);
-      if (!ctl->abort) {
+      // this CTA's share of the routed units: segments of (active expert, unit range); then release the producer
+      auto plan = [&]() {
+        const int U = ctl->U, N = U * I;
+        const int lo = range_lo(N, cta, G), hi = range_lo(N, cta + 1, G);
+        int nseg = 0;
 #pragma unroll 1
-        for (int t = rt; t < T; t += RW) {
-          const float* lg = a.logits + (size_t)t * (E + 1);
-          int my_idx;
-          float my_logit;
-          warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit, a.ex_gu, L.exgu_expert, a.ex_dn,
-                                   L.exdn_expert);
-          const float mx = __shfl_sync(FULL, my_logit, 0);
-          const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
-          const float Z = warp_sum(ex);
+        for (int aa = lo / I; aa * I < hi && lo < hi; ++aa) {
+          if (nseg == DEC_MAXSEG) { set_error(a, ctl, ERR_SEGMENTS); break; }
+          ctl->seg_a[nseg] = aa;
+          ctl->seg_u0[nseg] = max(lo, aa * I) - aa * I;
+          ctl->seg_u1[nseg] = min(hi, (aa + 1) * I) - aa * I;
+          ++nseg;
+        }
+        ctl->nseg = ctl->abort ? 0 : nseg;
+        mbar_arrive(&ctl->route_ready);
+        stamp(a, 5);
+      };
+      // one token: every copy is issued right after routing and the ring holds them all, so an L2 prefetch
+      // would only queue ahead of them; with more tokens the ring wraps and the prefetch warms L2
+      const uint8_t* pf_gu = ONE ? nullptr : a.ex_gu;
+      const size_t dn0 = (size_t)r0 * L.DR, dn1 = (size_t)r1 * L.DR;
+      if (ONE) {
+        // one token: the K experts in selection order are the active experts, one pair each
+        const float* lg = a.logits;
+        int my_idx = 0;
+        float my_logit = 0.f;
+        if (!ctl->abort)
+          warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit, pf_gu, L.exgu_expert, a.ex_dn, L.exdn_expert,
+                                   dn0, dn1);
+        if (rtid == 0) stamp(a, 4);
+        if (lane < K) {
+          ctl->act_e[lane] = (uint16_t)my_idx;
+          ctl->act_mask[lane] = 1u;
+          ctl->act_pb[lane] = (uint16_t)lane;
+          ctl->pair_tok[lane] = 0;
+          ctl->tok_pair[0][lane] = (uint8_t)lane;
+          ctl->ids[0][lane] = my_idx;
+        }
+        if (lane == 0) {
+          ctl->act_pb[K] = (uint16_t)K;
+          ctl->U = ctl->abort ? 0 : K;
+        }
+        __syncwarp();
+        if (lane == 0) plan();
+        // routing weights: needed only from the down projection on
+        const float mx = __shfl_sync(FULL, my_logit, 0);
+        const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
+        const float Z = warp_sum(ex);
+        const float wv = __fdividef(ex, Z);
+        if (lane < K) {
+          ctl->pair_w[lane] = wv;
+          ctl->wts[0][lane] = wv;
+        }
+        if (lane == 0) ctl->sg[0] = __frcp_rn(1.0f + __expf(-__ldcg(lg + E)));
+        if (cta == 0 && a.rec_ids) {
           int rank = 0;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -570,22 +687,39 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
             rank += (i < K && oi < my_idx) ? 1 : 0;
           }
           if (lane < K) {
-            ctl->ids[t][rank] = my_idx;
-            ctl->wts[t][rank] = __fdividef(ex, Z);
+            a.rec_ids[rank] = my_idx;
+            a.rec_w[rank] = wv;
           }
-          if (lane == 0) ctl->sg[t] = __frcp_rn(1.0f + __expf(-__ldcg(lg + E)));
+          if (lane == 0) a.rec_sg[0] = ctl->sg[0];
         }
-      }
-      named_bar(BAR_R, NT);
-      if (rtid == 0) stamp(a, 4);
-      // bucketing: token masks per expert, active experts in ascending order
-      if (T == 1) {
-        if (rtid < K) {
-          ctl->act_e[rtid] = (uint16_t)ctl->ids[0][rtid];
-          ctl->act_mask[rtid] = 1u;
-        }
-        if (rtid == 0) ctl->U = ctl->abort ? 0 : K;
       } else {
+        if (!ctl->abort) {
+#pragma unroll 1
+          for (int t = rt; t < T; t += RW) {
+            const float* lg = a.logits + (size_t)t * (E + 1);
+            int my_idx;
+            float my_logit;
+            warp_topk<(E + 31) / 32>(lg, E, K, lane, my_idx, my_logit, pf_gu, L.exgu_expert, a.ex_dn,
+                                     L.exdn_expert, dn0, dn1);
+            const float mx = __shfl_sync(FULL, my_logit, 0);
+            const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
+            const float Z = warp_sum(ex);
+            int rank = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int oi = __shfl_sync(FULL, my_idx, i);
+              rank += (i < K && oi < my_idx) ? 1 : 0;
+            }
+            if (lane < K) {
+              ctl->ids[t][rank] = my_idx;
+              ctl->wts[t][rank] = __fdividef(ex, Z);
+            }
+            if (lane == 0) ctl->sg[t] = __frcp_rn(1.0f + __expf(-__ldcg(lg + E)));
+          }
+        }
+        named_bar(BAR_R, NT);
+        if (rtid == 0) stamp(a, 4);
+        // bucketing: token masks per expert; active experts in ascending order with their first sorted pair
 #pragma unroll 1
         for (int e = rtid; e < E; e += NT) ctl->emask[e] = 0u;
         named_bar(BAR_R, NT);
@@ -594,24 +728,26 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
           for (int p = rtid; p < T * K; p += NT) atomicOr(&ctl->emask[ctl->ids[p / K][p % K]], 1u << (p / K));
         named_bar(BAR_R, NT);
         const int EPT = (E + NT - 1) / NT;
-        int cnt = 0;
+        int cnt = 0, pcnt = 0;
 #pragma unroll 1
         for (int q = 0; q < EPT; ++q) {
           const int e = rtid * EPT + q;
-          cnt += (e < E && ctl->emask[e] != 0u) ? 1 : 0;
+          const uint32_t msk = e < E ? ctl->emask[e] : 0u;
+          cnt += msk != 0u ? 1 : 0;
+          pcnt += __popc(msk);
         }
-        int incl = cnt;
+        int incl = cnt, pincl = pcnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(FULL, incl, o);
-          if (lane >= o) incl += v;
+          const int v = __shfl_up_sync(FULL, incl, o), pv = __shfl_up_sync(FULL, pincl, o);
+          if (lane >= o) { incl += v; pincl += pv; }
         }
-        if (lane == 31) ctl->warp_tot[rt] = incl;
+        if (lane == 31) { ctl->warp_tot[rt] = incl; ctl->warp_tot2[rt] = pincl; }
         named_bar(BAR_R, NT);
-        int base = 0;
+        int base = 0, pbase = 0;
 #pragma unroll 1
-        for (int w = 0; w < rt; ++w) base += ctl->warp_tot[w];
-        int pos = base + incl - cnt;
+        for (int w = 0; w < rt; ++w) { base += ctl->warp_tot[w]; pbase += ctl->warp_tot2[w]; }
+        int pos = base + incl - cnt, ppos = pbase + pincl - pcnt;
 #pragma unroll 1
         for (int q = 0; q < EPT; ++q) {
           const int e = rtid * EPT + q;
@@ -619,81 +755,65 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
           if (msk != 0u) {
             ctl->act_e[pos] = (uint16_t)e;
             ctl->act_mask[pos] = msk;
+            ctl->act_pb[pos] = (uint16_t)ppos;
             ++pos;
+            ppos += __popc(msk);
           }
         }
-        if (rtid == NT - 1) ctl->U = base + incl;
-      }
-      named_bar(BAR_R, NT);
-      const int U = ctl->U;
-      const int N = U * I;
-      if (rtid == 0) {
-        const int lo = range_lo(N, cta, G), hi = range_lo(N, cta + 1, G);
-        int nseg = 0;
+        if (rtid == NT - 1) {
+          ctl->U = ctl->abort ? 0 : base + incl;
+          ctl->act_pb[base + incl] = (uint16_t)(pbase + pincl);
+        }
+        named_bar(BAR_R, NT);
+        if (rtid == 0) plan();
+        // the sorted pairs: token and weight of each, and each token's pair per expert slot
+        const int U = ctl->U;
 #pragma unroll 1
-        for (int aa = lo / I; aa * I < hi && lo < hi; ++aa) {
-          if (nseg == DEC_MAXSEG) { set_error(a, ctl, ERR_SEGMENTS); break; }
+        for (int aa = rtid; aa < U; aa += NT) {
           const int e = ctl->act_e[aa];
-          const uint32_t msk = ctl->act_mask[aa];
-          ctl->seg_e[nseg] = e;
-          ctl->seg_u0[nseg] = max(lo, aa * I) - aa * I;
-          ctl->seg_u1[nseg] = min(hi, (aa + 1) * I) - aa * I;
-          int n = 0;
+          uint32_t msk = ctl->act_mask[aa];
+          int p = ctl->act_pb[aa];
 #pragma unroll 1
-          for (int t = 0; t < T; ++t) {
-            if (msk & (1u << t)) {
-              ctl->seg_tok[nseg][n] = (uint8_t)t;
-              float wv = 0.f;
+          while (msk != 0u) {
+            const int t = __ffs(msk) - 1;
+            msk &= msk - 1u;
+            ctl->pair_tok[p] = (uint8_t)t;
 #pragma unroll 1
-              for (int j = 0; j < K; ++j)
-                if (ctl->ids[t][j] == e) wv = ctl->wts[t][j];
-              ctl->seg_w[nseg][n] = wv;
-              ++n;
-            }
+            for (int j = 0; j < K; ++j)
+              if (ctl->ids[t][j] == e) {
+                ctl->pair_w[p] = ctl->wts[t][j];
+                ctl->tok_pair[t][j] = (uint8_t)p;
+              }
+            ++p;
           }
-          ctl->seg_n[nseg] = n;
-          const int units = ctl->seg_u1[nseg] - ctl->seg_u0[nseg];
-          if (units * n > hseg_floats) set_error(a, ctl, ERR_HSEG);
-          ++nseg;
         }
-        ctl->nseg = ctl->abort ? 0 : nseg;
-        mbar_arrive(&ctl->route_ready);
-        stamp(a, 5);
-      }
-      // off the critical path: every CTA's segment table and, per token, the list of partial-sum slots that
-      // hold it (final reduction)
+        if (cta == 0 && a.rec_ids) {
 #pragma unroll 1
-      for (int c = rtid; c < G; c += NT) {
-        const int lo = range_lo(N, c, G), hi = range_lo(N, c + 1, G);
-        ctl->tab_a0[c] = (uint16_t)(lo / I);
-        ctl->tab_n[c] = (uint8_t)(lo < hi ? (hi - 1) / I - lo / I + 1 : 0);
-      }
-
-      if (cta == 0 && a.rec_ids) {
+          for (int p = rtid; p < T * K; p += NT) {
+            a.rec_ids[p] = ctl->ids[p / K][p % K];
+            a.rec_w[p] = ctl->wts[p / K][p % K];
+          }
 #pragma unroll 1
-        for (int p = rtid; p < T * K; p += NT) {
-          a.rec_ids[p] = ctl->ids[p / K][p % K];
-          a.rec_w[p] = ctl->wts[p / K][p % K];
+          for (int t = rtid; t < T; t += NT) a.rec_sg[t] = ctl->sg[t];
         }
-#pragma unroll 1
-        for (int t = rtid; t < T; t += NT) a.rec_sg[t] = ctl->sg[t];
       }
     }
     named_bar(BAR_C, CT);
 
-    // ---- C: shared down rows (every CTA's hs; the routed weights are in flight meanwhile)
+    // ---- C: the shared expert's down projection for this CTA's output rows (every CTA's hs); its weights came
+    // in before routing, and it runs while the routed weights are still on their way
     if (ctid == 0 && !ctl->abort && !spin_geq(&a.counters[1], (uint32_t)G, a.timeout_ns))
       set_error(a, ctl, ERR_WAIT_HS);
     named_bar(BAR_C, CT);
     if (!ctl->abort)
 #pragma unroll 1
       for (int i = ctid; i < T * Is / 4; i += CT)
-        reinterpret_cast<float4*>(hsn)[i] = __ldcg(reinterpret_cast<const float4*>(a.hs) + i);
+        reinterpret_cast<float4*>(hst)[i] = __ldcg(reinterpret_cast<const float4*>(a.hs) + i);
     named_bar(BAR_C, CT);
     if (!ctl->abort)
 #pragma unroll 1
       for (int i = ctid; i < T * (Is / 16); i += CT) {
-        const float4* src = reinterpret_cast<const float4*>(hsn + (size_t)i * 16);
+        const float4* src = reinterpret_cast<const float4*>(hst + (size_t)i * 16);
         const float4 p0 = src[0], p1 = src[1], p2 = src[2], p3 = src[3];
         hss[i] = ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w)) +
                  ((p2.x + p2.y) + (p2.z + p2.w)) + ((p3.x + p3.y) + (p3.z + p3.w));
@@ -726,7 +846,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
 #pragma unroll
               for (int tt = 0; tt < TK; ++tt) {
                 if (tt < nt) {
-                  const float4* hv = reinterpret_cast<const float4*>(hsn + (size_t)(tc + tt) * Is + cc * 16);
+                  const float4* hv = reinterpret_cast<const float4*>(hst + (size_t)(tc + tt) * Is + cc * 16);
                   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                   for (int m = 0; m < 4; ++m) {
@@ -742,23 +862,22 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
             for (int tt = 0; tt < TK; ++tt) rs[tt] = warp_sum(rs[tt]);
             if (lane == 0)
 #pragma unroll 1
-              for (int tt = 0; tt < nt; ++tt) shs[(tc + tt) * (r1 - r0) + (r + rr - r0)] = rs[tt];
+              for (int tt = 0; tt < nt; ++tt) shs[(tc + tt) * nrow + (r + rr - r0)] = rs[tt];
           }
         }
       }
       release();
     }
-    named_bar(BAR_C, CT);
     if (ctid == 0) stamp(a, 10);
 
-    // ---- B: routed segments
+    // ---- B1: routed gate/up -> h of every (expert, token) pair, to global (row per sorted pair)
     const int nseg = ctl->nseg;
 #pragma unroll 1
     for (int sgi = 0; sgi < nseg; ++sgi) {
-      const int u0 = ctl->seg_u0[sgi], u1 = ctl->seg_u1[sgi], ne = ctl->seg_n[sgi];
-      const int units = u1 - u0;
-      const uint8_t* toks = ctl->seg_tok[sgi];
-      // gate/up -> h, a pair of units per warp
+      const int aa = ctl->seg_a[sgi], u0 = ctl->seg_u0[sgi], u1 = ctl->seg_u1[sgi];
+      const int pb = ctl->act_pb[aa], ne = ctl->act_pb[aa + 1] - pb;
+      const uint8_t* toks = ctl->pair_tok + pb;
+      float* hrow = a.hbuf + (size_t)pb * I;
       if (sgi == 0) wstamp(a, cw, 0);
 #pragma unroll 1
       for (int u = u0; u < u1; u += UPI) {
@@ -769,10 +888,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
           const int pbase = (u - u0) >> 1;
 #pragma unroll 1
           for (int pr = (cw - pbase % NCW + NCW) % NCW; pr * 2 < nu; pr += NCW) {
-            if (sgi == 0) wstamp(a, cw, 1);
             const uint8_t* ub = st + (size_t)(2 * pr) * L.EU;
             const int nvalid = (2 * pr + 1 < nu) ? 4 : 2;
-            const int ul = u + 2 * pr - u0;
+            const int ui = u + 2 * pr;
 #pragma unroll 1
             for (int tc = 0; tc < ne; tc += TK) {
               const int nt = min(TK, ne - tc);
@@ -786,190 +904,201 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
 #pragma unroll
                 for (int q = 0; q < TK; ++q)
                   if (q == tt) { g = k ? d.v[q][2] : d.v[q][0]; up = k ? d.v[q][3] : d.v[q][1]; }
-                if (tt < nt && 2 * k < nvalid) hseg[(tc + tt) * units + ul + k] = silu_fast(g) * up;
+                if (tt < nt && 2 * k < nvalid) hrow[(size_t)(tc + tt) * I + hpos<I>(ui + k)] = silu_fast(g) * up;
               }
             }
-            if (sgi == 0) wstamp(a, cw, 2);
           }
         }
         release();
       }
-      named_bar(BAR_C, CT);
-      if (ctid == 0 && sgi == 0) stamp(a, 7);
-      if (sgi == 0) wstamp(a, cw, 3);
-      // down: per group, the (s,b) block then the unit columns; each thread owns 4 output rows
-      const int hq = ctid;
-      const bool has_q = hq < H / 4;
-      const bool in_regs = ne <= TK;   // all tokens' partial sums stay in registers across the segment
-      float4 pacc[TK];
-#pragma unroll
-      for (int tt = 0; tt < TK; ++tt) pacc[tt] = make_float4(0.f, 0.f, 0.f, 0.f);
-      bool first = true;
-      const size_t slot0 = ((size_t)cta * DEC_MAXSEG + sgi) * T;
-#pragma unroll 1
-      for (int g = u0 / 64; g * 64 < u1; ++g) {
-        float2 sbq[4];
-        {
-          const uint8_t* st = acquire();
-          if (!ctl->abort && has_q) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(st + (size_t)hq * 16);
-            sbq[0] = h2f(raw.x); sbq[1] = h2f(raw.y); sbq[2] = h2f(raw.z); sbq[3] = h2f(raw.w);
-          }
-          release();
-        }
-        const int ga = max(u0, g * 64), gb = min(u1, g * 64 + 64);
-#pragma unroll 1
-        for (int u = ga; u < gb; u += DPI) {
-          const int nu = min(DPI, gb - u);
-          const uint8_t* st = acquire();
-          if (!ctl->abort && has_q) {
-#pragma unroll 1
-            for (int tc = 0; tc < ne; tc += TK) {
-              const int nt = min(TK, ne - tc);
-              float2 acc[TK][2];
-              float hsum[TK];
-#pragma unroll
-              for (int tt = 0; tt < TK; ++tt) {
-                acc[tt][0] = acc[tt][1] = make_float2(0.f, 0.f);
-                hsum[tt] = 0.f;
-              }
-              const float* hrow = hseg + (size_t)tc * units + (u - u0);
-#pragma unroll 4
-              for (int k = 0; k < nu; ++k) {
-                const uint32_t hw = *reinterpret_cast<const uint16_t*>(st + (size_t)k * L.DCB + hq * 2);
-                float2 q01, q23;
-                unpack_int4_quad(hw, q01, q23);
-#pragma unroll
-                for (int tt = 0; tt < TK; ++tt) {
-                  if (tt < nt) {
-                    const float h = hrow[tt * units + k];
-                    acc[tt][0] = __ffma2_rn(q01, make_float2(h, h), acc[tt][0]);
-                    acc[tt][1] = __ffma2_rn(q23, make_float2(h, h), acc[tt][1]);
-                    hsum[tt] += h;
-                  }
-                }
-              }
-#pragma unroll
-              for (int tt = 0; tt < TK; ++tt) {
-                if (tt < nt) {
-                  const float w = ctl->seg_w[sgi][tc + tt];
-                  float4 v;
-                  v.x = w * (sbq[0].x * acc[tt][0].x + sbq[0].y * hsum[tt]);
-                  v.y = w * (sbq[1].x * acc[tt][0].y + sbq[1].y * hsum[tt]);
-                  v.z = w * (sbq[2].x * acc[tt][1].x + sbq[2].y * hsum[tt]);
-                  v.w = w * (sbq[3].x * acc[tt][1].y + sbq[3].y * hsum[tt]);
-                  if (in_regs) {
-                    pacc[tt].x += v.x; pacc[tt].y += v.y; pacc[tt].z += v.z; pacc[tt].w += v.w;
-                  } else {
-                    float4* dst = reinterpret_cast<float4*>(a.partial + (slot0 + tc + tt) * H + 4 * hq);
-                    if (!first) {
-                      const float4 o = __ldcg(dst);
-                      v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-                    }
-                    __stcg(dst, v);
-                  }
-                }
-              }
-            }
-          }
-          first = false;
-          release();
-        }
-      }
-      if (in_regs && !ctl->abort && has_q) {
-#pragma unroll
-        for (int tt = 0; tt < TK; ++tt)
-          if (tt < ne) __stcg(reinterpret_cast<float4*>(a.partial + (slot0 + tt) * H + 4 * hq), pacc[tt]);
-      }
-      named_bar(BAR_C, CT);
+      if (sgi == 0) wstamp(a, cw, 1);
     }
-    if (ctid == 0) stamp(a, 8);
-
-    // ---- D: all partials finished -> fixed-order reduction of this CTA's rows
+    named_bar(BAR_C, CT);
     if (ctid == 0) {
+      stamp(a, 7);
       __threadfence();
       atomicAdd(&a.counters[2], 1u);
-      if (!ctl->abort && !spin_geq(&a.counters[2], (uint32_t)G, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_PARTIAL);
-      stamp(a, 11);
     }
-    // while thread 0 waits for every CTA: per token, the list of partial-sum slots that hold it
+
+
+    // ---- every CTA's routed h is in global memory
+    if (ctid == 0 && !ctl->abort && !spin_geq(&a.counters[2], (uint32_t)G, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_H);
+    if (ctid == 0) stamp(a, 11);
+
+    // ---- B2: routed down projection of this CTA's rows. Active experts go in batches whose pairs fit the h
+    // stage and whose items fit half the ring; a batch's items are all held at once and its (expert, row) dots
+    // are spread over the warps.
+    {
+      const int U = ctl->U;
+      const int lim = max(1, NS / dn_items);
+      constexpr int NPC = ONE ? 1 : 4;
+      int aa0 = 0;
+      if (ONE) {
+        // One token, U = K experts with one pair each, all their down items in the ring. Thread 0, which has
+        // just seen every CTA's h, copies all U h vectors (already in the dot's lane order) into shared memory
+        // with one bulk copy. A warp then takes one (expert, half of the CTA's rows): h into registers once,
+        // rows four at a time as independent chains, and one transposed reduction per four rows.
+        constexpr int NCL = (NC + 31) / 32;      // 16-column chunks per lane
+        const int half = (nrow + 1) / 2;
+        if (ctid == 0) {
+          if (!ctl->abort && U > 0) {
+            fence_proxy_async_global();
+            mbar_expect_tx(&ctl->hbar, (uint32_t)(U * I * 4));
+            bulk_g2s(hst, a.hbuf, (uint32_t)(U * I * 4), &ctl->hbar);
+          } else {
+            mbar_arrive(&ctl->hbar);
+          }
+        }
+        if (!ctl->abort && !mbar_wait(&ctl->hbar, 0, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_FULL);
+        wstamp(a, cw, 2);
 #pragma unroll 1
-      for (int t = cw - 1; cw > 0 && t < T; t += NCW - 1) {
-        int n = 0;
-#pragma unroll 1
-        for (int c0 = 0; c0 < G; c0 += 32) {
-          const int c = c0 + lane;
-          uint32_t cnt = 0, sl[2] = {0u, 0u};
-          if (c < G) {
-            const int a0 = ctl->tab_a0[c], ns = min((int)ctl->tab_n[c], 2);
+        for (int wi = cw; wi < 2 * U; wi += NCW) {
+          const int aa = wi >> 1, rlo = (wi & 1) ? half : 0, rhi = (wi & 1) ? nrow : half;
+          float4 hv[NCL][4];
+          float hsum[NCL];
 #pragma unroll
-            for (int sg = 0; sg < 2; ++sg) {
-              if (sg < ns) {
-                const uint32_t msk = ctl->act_mask[a0 + sg];
-                if ((msk >> t) & 1u) {
-                  sl[cnt] = ((uint32_t)c * DEC_MAXSEG + sg) * T + __popc(msk & ((1u << t) - 1u));
-                  ++cnt;
-                }
+          for (int m = 0; m < NCL; ++m) {
+            const int c = lane + 32 * m;
+            hsum[m] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              hv[m][j] = (NC % 32 == 0 || c < NC) ? hst4[(size_t)aa * 4 * NC + j * NC + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+              hsum[m] += (hv[m][j].x + hv[m][j].y) + (hv[m][j].z + hv[m][j].w);
+            }
+          }
+#pragma unroll 1
+          for (int rg = rlo; rg < rhi; rg += 4) {
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              v[q] = 0.f;
+              const int rr = rg + q;
+              if (rr < rhi) {
+                const uint8_t* row = stage_at(aa * dn_items + rr / DRPI) + (size_t)(rr % DRPI) * L.DR;
+                if (!ctl->abort)
+#pragma unroll
+                  for (int m = 0; m < NCL; ++m) {
+                    const int c = lane + 32 * m;
+                    if (NC % 32 == 0 || c < NC) {
+                      const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+                      float2 qq[8];
+                      unpack_int4_quad(w.x & 0xFFFFu, qq[0], qq[1]);
+                      unpack_int4_quad(w.x >> 16, qq[2], qq[3]);
+                      unpack_int4_quad(w.y & 0xFFFFu, qq[4], qq[5]);
+                      unpack_int4_quad(w.y >> 16, qq[6], qq[7]);
+                      const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + I / 2 + (c >> 2) * 4));
+                      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                      for (int j = 0; j < 4; ++j) {
+                        acc = __ffma2_rn(qq[2 * j], make_float2(hv[m][j].x, hv[m][j].y), acc);
+                        acc = __ffma2_rn(qq[2 * j + 1], make_float2(hv[m][j].z, hv[m][j].w), acc);
+                      }
+                      v[q] += sb.x * (acc.x + acc.y) + sb.y * hsum[m];
+                    }
+                  }
               }
             }
+            // transposed reduction of the four values over the warp: lanes with bit 4 clear keep rows 0 and 1,
+            // the others rows 2 and 3; then bit 3 picks one of the pair; then a plain butterfly over 8 lanes
+            const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
+            float x0 = b4 ? v[2] : v[0], x1 = b4 ? v[3] : v[1];
+            const float y0 = b4 ? v[0] : v[2], y1 = b4 ? v[1] : v[3];
+            x0 += __shfl_xor_sync(FULL, y0, 16);
+            x1 += __shfl_xor_sync(FULL, y1, 16);
+            float z = b3 ? x1 : x0;
+            z += __shfl_xor_sync(FULL, b3 ? x0 : x1, 8);
+            z += __shfl_xor_sync(FULL, z, 4);
+            z += __shfl_xor_sync(FULL, z, 2);
+            z += __shfl_xor_sync(FULL, z, 1);
+            const int idx = lane >> 3;
+            if ((lane & 7) == 0 && rg + idx < rhi) yv[(size_t)aa * nrow + rg + idx] = z;
           }
-          uint32_t incl = cnt;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(FULL, incl, o);
-            if (lane >= o) incl += v;
-          }
-          const int pos = n + (int)(incl - cnt);
-          if (cnt > 0) ctl->slot[t][pos] = (uint16_t)sl[0];
-          if (cnt > 1) ctl->slot[t][pos + 1] = (uint16_t)sl[1];
-          n += (int)__shfl_sync(FULL, incl, 31);
         }
-        if (lane == 0) ctl->nslot[t] = n;
+        wstamp(a, cw, 3);
+#pragma unroll 1
+        for (int i = 0; i < U * dn_items; ++i) release();
+        aa0 = U;
       }
-    named_bar(BAR_C, CT);
-    if (!ctl->abort) {
-      const int nr = r1 - r0;
 #pragma unroll 1
-      for (int pi = cw; pi < T * nr; pi += NCW) {
-        const int t = pi / nr, rr = pi % nr, row = r0 + rr;
-        // every partial this lane needs is loaded before any is added (independent L2 reads in flight)
-        const int ns = ctl->nslot[t];
-        float v[2 * DEC_MAXGRID / 32];
+      while (aa0 < U) {
+        const int pb0 = ctl->act_pb[aa0];
+        int aa1 = aa0 + 1;
+#pragma unroll 1
+        while (aa1 < U && aa1 - aa0 < lim && ctl->act_pb[aa1 + 1] - pb0 <= hp) ++aa1;
+        const int np = ctl->act_pb[aa1] - pb0;
+        named_bar(BAR_C, CT);   // phase C and the previous batch no longer read the stage
+        if (!ctl->abort)
+#pragma unroll 1
+          for (int i = ctid; i < np * NC; i += CT) {
+            const int p = i / NC, c = i % NC;
+            const float4* src = reinterpret_cast<const float4*>(a.hbuf + (size_t)(pb0 + p) * I);
+            float s = 0.f;
 #pragma unroll
-        for (int k = 0; k < 2 * DEC_MAXGRID / 32; ++k) {
-          const int q = lane + 32 * k;
-          v[k] = q < ns ? __ldcg(a.partial + (size_t)ctl->slot[t][q] * H + row) : 0.f;
-        }
-        float acc = 0.f;
+            for (int j = 0; j < 4; ++j) {
+              const float4 v = __ldcg(src + j * NC + c);
+              hst4[(size_t)p * 4 * NC + j * NC + c] = v;
+              s += (v.x + v.y) + (v.z + v.w);
+            }
+            hsm[p * NC + c] = s;
+          }
+        named_bar(BAR_C, CT);
+        if (aa0 == 0) wstamp(a, cw, 2);
+        const int nit = (aa1 - aa0) * dn_items, nwork = (aa1 - aa0) * nrow;
+#pragma unroll 1
+        for (int wu = cw; wu < nwork; wu += NCW) {
+          const int ai = wu / nrow, rr = wu % nrow;
+          const uint8_t* st = stage_at(ai * dn_items + rr / DRPI);
+          if (!ctl->abort) {
+            const uint8_t* rowp = st + (size_t)(rr % DRPI) * L.DR;
+            const int pa = ctl->act_pb[aa0 + ai] - pb0, na = ctl->act_pb[aa0 + ai + 1] - pb0 - pa;
+#pragma unroll 1
+            for (int pc = 0; pc < na; pc += NPC) {
+              float y[NPC];
+              dot_down<I, NPC>(rowp, hst4, hsm, pa + pc, min(NPC, na - pc), y);
+              if (lane == 0)
 #pragma unroll
-        for (int k = 0; k < 2 * DEC_MAXGRID / 32; ++k) acc += v[k];
-        // rare: a CTA whose unit range touches more than two experts
-#pragma unroll 1
-        for (int c = lane; c < G; c += 32) {
-          const int a0 = ctl->tab_a0[c], ns = ctl->tab_n[c];
-#pragma unroll 1
-          for (int sg = 2; sg < ns; ++sg) {
-            const uint32_t msk = ctl->act_mask[a0 + sg];
-            if ((msk >> t) & 1u) {
-              const int tl = __popc(msk & ((1u << t) - 1u));
-              acc += __ldcg(a.partial + (((size_t)c * DEC_MAXSEG + sg) * T + tl) * H + row);
+                for (int pp = 0; pp < NPC; ++pp)
+                  if (pp < na - pc) yv[(size_t)(pb0 + pa + pc + pp) * nrow + rr] = y[pp];
             }
           }
         }
-        acc = warp_sum(acc);
-        if (lane == 0) {
-          float v = acc + ctl->sg[t] * shs[t * nr + rr];
-          if (a.gamma) v += __half2float(__ushort_as_half(a.x[(size_t)t * H + row]));
-          a.out[(size_t)t * H + row] = __half_as_ushort(__float2half_rn(v));
-        }
+        if (aa0 == 0) wstamp(a, cw, 3);
+#pragma unroll 1
+        for (int i = 0; i < nit; ++i) release();
+        aa0 = aa1;
       }
     }
+    named_bar(BAR_C, CT);
+    if (ctid == 0) stamp(a, 8);
+
+    // ---- D: out = sum over the token's experts (fixed order) of w * y + sigmoid(g) * shared (+ residual)
+    if (!ctl->abort)
+#pragma unroll 1
+      for (int i = ctid; i < T * nrow; i += CT) {
+        const int t = i / nrow, rr = i % nrow;
+        float acc = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < K; ++j) acc += ctl->wts[t][j] * yv[(size_t)ctl->tok_pair[t][j] * nrow + rr];
+        float v = acc + ctl->sg[t] * shs[t * nrow + rr];
+        if (a.gamma) v += __half2float(__ushort_as_half(a.x[(size_t)t * H + r0 + rr]));
+        a.out[(size_t)t * H + r0 + rr] = __half_as_ushort(__float2half_rn(v));
+      }
     named_bar(BAR_C, CT);
   }
 
   __syncthreads();
+  if (a.trace) {
+    if (threadIdx.x == 0) {
+      stamp(a, 12);
+      ctl->tclk[31] = globaltimer();
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) a.trace[cta * 32 + threadIdx.x] = ctl->tclk[threadIdx.x];
+    else if (threadIdx.x < 32 + NCW * 4)
+      a.trace[G * 32 + (cta * 16 + (threadIdx.x - 32) / 4) * 4 + (threadIdx.x - 32) % 4] =
+          ctl->wclk[(threadIdx.x - 32) / 4][(threadIdx.x - 32) % 4];
+  }
   if (threadIdx.x == 0) {
-    stamp(a, 12);
     __threadfence();
     const uint32_t prev = atomicAdd(&a.counters[3], 1u);
     if (prev == (uint32_t)G - 1) {
@@ -980,44 +1109,30 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
   }
 }
 
-template <int H>
-int hseg_bound(const MoeLayout& L, int T, int grid) {
-  int best = 0;
-  const int TK = T * L.K;
-#pragma unroll 1
-  for (int n = 1; n <= T; ++n) {
-    long long U = (long long)TK - n + 1;
-    if (U > L.E) U = L.E;
-    long long units = (U * L.I + grid - 1) / grid + 1;
-    if (units > L.I) units = L.I;
-    long long v = units * n;
-    if (v > best) best = (int)v;
-  }
-  return best;
-}
-
 }  // namespace
 
-size_t decode_partial_floats(const MoeLayout& L, int grid, int T) {
-  return (size_t)grid * DEC_MAXSEG * T * L.H;
-}
+size_t decode_hbuf_floats(const MoeLayout& L, int T) { return (size_t)T * L.K * L.I; }
 
 bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch* out) {
-  if (grid > DEC_MAXGRID) return false;
+  if (grid > DEC_MAXGRID || T < 1 || T > DEC_TMAX) return false;
+  const int rows = (L.H + grid - 1) / grid;
+  if (rows > DEC_MAXROWS) return false;
   DecodeLaunch pl;
   pl.grid = grid;
-  pl.hseg_floats = hseg_bound<0>(L, T, grid);
-  const Smem m = smem_map(L, T, grid, pl.hseg_floats);
-  const int upi = T <= 4 ? 8 : 4;
-  int SS = (int)(upi * L.EU);
+  pl.hp = T == 1 ? L.K : DEC_HP;
+  const Smem m = smem_map(L, T, grid, pl.hp);
+  int SS = (int)(4 * L.EU);
   if (SS < 4 * L.H) SS = 4 * L.H;
   if ((int)(2 * L.SU) > SS) SS = (int)(2 * L.SU);
   if ((int)L.RR > SS) SS = (int)L.RR;
   if ((int)L.SDR > SS) SS = (int)L.SDR;
+  if ((int)L.DR > SS) SS = (int)L.DR;
   SS = (SS + 127) & ~127;
   int NS = (max_smem - m.ring) / SS;
   if (NS > DEC_MAXNS) NS = DEC_MAXNS;
-  if (NS < 3) return false;
+  if (NS < 4) return false;
+  const int drpi = SS / (int)L.DR, dn_items = (rows + drpi - 1) / drpi;
+  if (dn_items > NS / 2) return false;
   pl.NS = NS;
   pl.SS = SS;
   pl.smem = m.ring + NS * SS;
@@ -1041,12 +1156,16 @@ static cudaError_t launch_s(const DecodeArgs& a, const DecodeLaunch& pl, cudaStr
   cfg.blockDim = dim3(DEC_THREADS);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
+  // The grid-wide counters need every CTA resident at once: one CTA per SM (its shared memory admits no
+  // second) and grid <= SM count guarantee it once the SMs are free. The launch is programmatic-dependent
+  // rather than cooperative: a dependent grid can start only after every CTA of this one has run
+  // launch_dependents, so it never holds an SM that a CTA of this grid still waits for.
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, pl.NS, pl.SS, pl.hseg_floats);
+  return cudaLaunchKernelEx(&cfg, kern, a, pl.NS, pl.SS, pl.hp);
 }
 
 template <class SH>

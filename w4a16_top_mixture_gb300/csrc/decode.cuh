@@ -10,13 +10,15 @@ constexpr int DEC_NCW = 16;                       // consumer warps
 constexpr int DEC_THREADS = (DEC_NCW + 1) * 32;   // + one producer warp
 constexpr int DEC_TMAX = 16;                      // largest T of the fused decode kernel
 constexpr int DEC_MAXSEG = 4;                     // expert segments one CTA's unit range may touch
+constexpr int DEC_MAXROWS = 32;                   // output rows one CTA owns (ceil(H / grid))
+constexpr int DEC_HP = 16;                        // routed h vectors staged in shared memory at once (T > 1)
 constexpr int DEC_MAXNS = 24;                     // ring stages
 constexpr int DEC_MAXGRID = 160;                  // CTAs (one per SM)
 
 // device error bits
 enum : uint32_t {
-  ERR_WAIT_LOGITS = 1u, ERR_WAIT_HS = 2u, ERR_WAIT_PARTIAL = 4u, ERR_WAIT_FULL = 8u, ERR_WAIT_EMPTY = 16u,
-  ERR_WAIT_ROUTE = 32u, ERR_SEGMENTS = 64u, ERR_HSEG = 128u,
+  ERR_WAIT_LOGITS = 1u, ERR_WAIT_HS = 2u, ERR_WAIT_H = 4u, ERR_WAIT_FULL = 8u, ERR_WAIT_EMPTY = 16u,
+  ERR_WAIT_ROUTE = 32u, ERR_SEGMENTS = 64u,
 };
 
 struct DecodeArgs {
@@ -28,7 +30,7 @@ struct DecodeArgs {
   int T;
   float* logits;            // [T][E+1]
   float* hs;                // [T][Is]
-  float* partial;           // [G*MAXSEG*T][H]
+  float* hbuf;              // [T*K][I] routed h, one row per (expert, token) pair in expert-sorted order
   uint32_t* counters;       // [4]
   uint32_t* status;
   int32_t* rec_ids;         // routing record [T][K] (written by CTA 0)
@@ -40,13 +42,13 @@ struct DecodeArgs {
 };
 
 struct DecodeLaunch {
-  int grid, smem, NS, SS, hseg_floats;
+  int grid, smem, NS, SS, hp;   // hp: routed h vectors the shared-memory stage holds
 };
 
 // Host: shared-memory plan for a call with T tokens; returns false if it does not fit.
 bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch* out);
 bool decode_supported(const MoeLayout& L);   // shapes with a compiled decode kernel
 cudaError_t decode_launch(const MoeLayout& L, const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st);
-size_t decode_partial_floats(const MoeLayout& L, int grid, int T);
+size_t decode_hbuf_floats(const MoeLayout& L, int T);
 
 }  // namespace moe

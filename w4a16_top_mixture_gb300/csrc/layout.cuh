@@ -7,9 +7,8 @@
 //   sh_gu    [Is][SU]      unit i: gate row codes (permuted) | up row codes (permuted) | gate (s,b) | up (s,b)
 //   sh_dn    [H][SDR]      row r: Is int8 codes in natural order | Is/64 (s,b)
 //   ex_gu    [E][I][EU]    unit (e,i): gate row int4 codes | up row int4 codes | gate (s,b) | up (s,b)
-//   ex_dn    [E][I/64][DB] per (expert, group of 64 intermediate units): (s,b) of every output row (H pairs),
-//                          then 64 units, each the unit's COLUMN of the down matrix as H int4 codes, two per
-//                          byte (row 2m in the low nibble of byte m)
+//   ex_dn    [E][H][DR]    row r of expert e's down matrix: I int4 codes in canonical packing | I/64 (s,b);
+//                          a CTA's output rows of one expert are one contiguous range
 //
 // Row codes of int4 matrices keep the canonical packing. int8 rows are permuted in 16-byte blocks so that the
 // lanes of a warp read consecutive 16 bytes: the 32-column chunk c = l + LW*p, half h (16 columns), lands at
@@ -32,7 +31,7 @@ struct MoeLayout {
   int H, E, K, I, Is;
   int GB, GI, GS;     // groups of 64 along H, I, Is
   int NCH, LW, P;     // 32-column chunks per H row, lanes per row, chunks per lane
-  size_t RR, SU, SDR, EU, DSB, DCB, DB;
+  size_t RR, SU, SDR, EU, DR;
   size_t router_bytes, shgu_bytes, shdn_bytes, exgu_bytes, exdn_bytes;
   size_t exgu_expert, exdn_expert;
 };
@@ -46,14 +45,12 @@ inline MoeLayout moe_make_layout(int H, int E, int K, int I, int Is) {
   L.SU = moe_align16(2 * (size_t)H + 2 * (size_t)L.GB * 4);
   L.SDR = moe_align16((size_t)Is + (size_t)L.GS * 4);
   L.EU = moe_align16((size_t)H + 2 * (size_t)L.GB * 4);
-  L.DSB = (size_t)H * 4;
-  L.DCB = (size_t)H / 2;
-  L.DB = L.DSB + 64 * L.DCB;
+  L.DR = moe_align16((size_t)I / 2 + (size_t)L.GI * 4);
   L.router_bytes = (size_t)(E + 1) * L.RR;
   L.shgu_bytes = (size_t)Is * L.SU;
   L.shdn_bytes = (size_t)H * L.SDR;
   L.exgu_expert = (size_t)I * L.EU;
-  L.exdn_expert = (size_t)L.GI * L.DB;
+  L.exdn_expert = (size_t)H * L.DR;
   L.exgu_bytes = (size_t)E * L.exgu_expert;
   L.exdn_bytes = (size_t)E * L.exdn_expert;
   return L;

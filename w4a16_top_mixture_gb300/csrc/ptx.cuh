@@ -24,6 +24,11 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// orders this thread's earlier generic-proxy view of global memory before its later async-proxy (bulk copy)
+// reads of global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -154,7 +159,8 @@ __device__ __forceinline__ void unpack_int8_word(uint32_t w, float2& q01, float2
   q23 = __ffma2_rn(f2(bits((h & 0xFFu) | MAGIC), bits((h & 0xFF00u) | MAGIC)), f2(1.f, s8), f2(-8388608.0f, -32768.0f));
 }
 
-// Four int4 codes of a 16-bit field (rows 4m..4m+3 of a down-matrix column) -> (q0, q1), (q2, q3), exact.
+// Four int4 codes of a 16-bit field (columns 4m..4m+3 of a canonically packed int4 row) -> (q0, q1), (q2, q3),
+// exact.
 __device__ __forceinline__ void unpack_int4_quad(uint32_t hw, float2& q01, float2& q23) {
   const float a = bits((hw & 0xFu) | MAGIC), b = bits((hw & 0xF0u) | MAGIC);
   const float c = bits((hw & 0xF00u) | MAGIC), d = bits((hw & 0xF000u) | MAGIC);

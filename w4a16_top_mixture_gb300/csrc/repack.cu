@@ -46,37 +46,6 @@ __global__ void k_repack_int4_rows(const uint8_t* __restrict__ q, const uint16_t
   }
 }
 
-// Expert down matrices [E][H][I/2] -> per (expert, group): (s,b) of all H rows, then 64 columns of H codes.
-__global__ void k_repack_down(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s,
-                              const uint16_t* __restrict__ b, uint8_t* __restrict__ dst, int E, int H, int I,
-                              size_t DB, size_t DSB) {
-  const int GI = I / 64;
-  size_t n_code_bytes = (size_t)E * I * (H / 2);        // one output byte = rows (2m, 2m+1) of a column
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_code_bytes;
-       i += (size_t)gridDim.x * blockDim.x) {
-    int m = (int)(i % (H / 2));
-    size_t t = i / (H / 2);
-    int col = (int)(t % I);
-    int e = (int)(t / I);
-    int g = col / 64, u = col % 64;
-    const uint8_t* src = q + (size_t)e * H * (I / 2);
-    int r0 = 2 * m, r1 = 2 * m + 1;
-    uint32_t n0 = (src[(size_t)r0 * (I / 2) + col / 2] >> (4 * (col & 1))) & 0xF;
-    uint32_t n1 = (src[(size_t)r1 * (I / 2) + col / 2] >> (4 * (col & 1))) & 0xF;
-    uint8_t* blk = dst + ((size_t)e * GI + g) * DB;
-    blk[DSB + (size_t)u * (H / 2) + m] = (uint8_t)(n0 | (n1 << 4));
-  }
-  size_t n_sb = (size_t)E * H * GI;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_sb; i += (size_t)gridDim.x * blockDim.x) {
-    int g = (int)(i % GI);
-    size_t t = i / GI;
-    int r = (int)(t % H);
-    int e = (int)(t / H);
-    uint8_t* blk = dst + ((size_t)e * GI + g) * DB;
-    *reinterpret_cast<uint32_t*>(blk + (size_t)r * 4) = sb_pair(s, b, i);
-  }
-}
-
 // ---------------------------------------------------------------- debug dequantisation
 // which: 0 router, 1 expert gate, 2 expert up, 3 expert down, 4 shared gate, 5 shared up, 6 shared down.
 // Output row-major in the canonical orientation. Every element goes through the forward kernels' unpack
@@ -112,31 +81,27 @@ __global__ void k_debug_dequant(const uint8_t* __restrict__ base, MoeLayout L, i
         v[k] = __fmaf_rn(sb.x, f.x - 1024.0f, sb.y);
         v[4 + k] = __fmaf_rn(sb.x, f.y - 1024.0f, sb.y);
       }
-    } else if (which == 1 || which == 2) {
-      const uint8_t* unit = base + ((size_t)index * L.I + r) * L.EU;
-      const uint8_t* row = unit + (which == 2 ? L.H / 2 : 0);
-      size_t sb_off = (size_t)L.H + (which == 2 ? (size_t)L.GB * 4 : 0);
+    } else if (which >= 1 && which <= 3) {
+      // int4 rows: expert gate / up (units of gate row | up row | pairs) or down (row | pairs)
+      const uint8_t* row;
+      const uint8_t* sbp;
+      if (which == 3) {
+        row = base + ((size_t)index * L.H + r) * L.DR;
+        sbp = row + L.I / 2;
+      } else {
+        const uint8_t* unit = base + ((size_t)index * L.I + r) * L.EU;
+        row = unit + (which == 2 ? L.H / 2 : 0);
+        sbp = unit + (size_t)L.H + (which == 2 ? (size_t)L.GB * 4 : 0);
+      }
       uint32_t w = *reinterpret_cast<const uint32_t*>(row + c8 / 2);
       uint32_t pr[4];
       int4_word_pairs(w, pr);
-      float2 sb = h2f(*reinterpret_cast<const uint32_t*>(unit + sb_off + (c8 / 64) * 4));
+      float2 sb = h2f(*reinterpret_cast<const uint32_t*>(sbp + (c8 / 64) * 4));
       for (int k = 0; k < 4; ++k) {
         const float2 f = h2f(pr[k]);   // 1024 + q (k even) or 1024 + 16 q (k odd), exactly
         const float sc = (k & 1) ? 0.0625f : 1.0f;
         v[k] = __fmaf_rn(sb.x, (f.x - 1024.0f) * sc, sb.y);
         v[4 + k] = __fmaf_rn(sb.x, (f.y - 1024.0f) * sc, sb.y);
-      }
-    } else if (which == 3) {
-      // row r of the down matrix: column c of group g sits in block (index, g), unit c%64, quad r/4
-      for (int cc = 0; cc < 8; ++cc) {
-        int c = c8 + cc, g = c / 64, u = c % 64;
-        const uint8_t* blk = base + ((size_t)index * L.GI + g) * L.DB;
-        uint32_t hw = *reinterpret_cast<const uint16_t*>(blk + L.DSB + (size_t)u * L.DCB + (r / 4) * 2);
-        float2 q01, q23;
-        unpack_int4_quad(hw, q01, q23);
-        float qs[4] = {q01.x, q01.y, q23.x, q23.y};
-        float2 sb = h2f(*reinterpret_cast<const uint32_t*>(blk + (size_t)r * 4));
-        v[cc] = __fmaf_rn(sb.x, qs[r % 4], sb.y);
       }
     } else {
       const uint8_t* row = base + (size_t)r * L.SDR;
@@ -182,8 +147,9 @@ cudaError_t repack_all(const RepackSrc& w, const MoeLayout& L, const RepackDst& 
   k_repack_int4_rows<<<grid_for((size_t)E * I * H / 2), 256, 0, st>>>(w.exp_up_q, w.exp_up_s, w.exp_up_b, d.ex_gu,
                                                                        E * I, H, L.EU, H / 2,
                                                                        (size_t)H + (size_t)L.GB * 4);
-  k_repack_down<<<grid_for((size_t)E * I * H / 2), 256, 0, st>>>(w.exp_down_q, w.exp_down_s, w.exp_down_b, d.ex_dn,
-                                                                  E, H, I, L.DB, L.DSB);
+  // expert down rows: rows of all experts are consecutive (e*H + r)
+  k_repack_int4_rows<<<grid_for((size_t)E * H * I / 2), 256, 0, st>>>(w.exp_down_q, w.exp_down_s, w.exp_down_b,
+                                                                       d.ex_dn, E * H, I, L.DR, 0, I / 2);
   return cudaGetLastError();
 }
 

@@ -213,7 +213,12 @@ class MoeBlock:
         _check(self.lib.moe_block_debug_set_wait(self.h, int(timeout_us), int(bool(skip_arrive))), "set_wait")
 
     def set_trace(self, buf=None):
-        """buf: int64 CUDA tensor of >= 32 * SM-count entries, or None to stop tracing."""
+        """buf: int64 CUDA tensor of >= 96 * SM-count entries, or None to stop tracing."""
+        if buf is not None:
+            import torch
+            sms = torch.cuda.get_device_properties(buf.device).multi_processor_count
+            if buf.dtype != torch.int64 or buf.numel() < 96 * sms or not buf.is_contiguous():
+                raise ValueError(f"trace buffer must be a contiguous int64 tensor of >= {96 * sms} entries")
         _check(self.lib.moe_block_debug_set_trace(self.h, _ptr(buf)), "set_trace")
 
     def last_launch_count(self):
