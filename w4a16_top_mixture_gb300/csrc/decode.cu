@@ -966,6 +966,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
               hsum[m] += (hv[m][j].x + hv[m][j].y) + (hv[m][j].z + hv[m][j].w);
             }
           }
+          // the expert's rows of this CTA: one ring item when they fit a stage (always, at production width)
+          const uint8_t* item0 = dn_items == 1 ? stage_at(aa) : nullptr;
 #pragma unroll 1
           for (int rg = rlo; rg < rhi; rg += 4) {
             float v[4];
@@ -974,7 +976,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
               v[q] = 0.f;
               const int rr = rg + q;
               if (rr < rhi) {
-                const uint8_t* row = stage_at(aa * dn_items + rr / DRPI) + (size_t)(rr % DRPI) * L.DR;
+                const uint8_t* row = item0 ? item0 + rr * (int)L.DR
+                                           : stage_at(aa * dn_items + rr / DRPI) + (size_t)(rr % DRPI) * L.DR;
                 if (!ctl->abort)
 #pragma unroll
                   for (int m = 0; m < NCL; ++m) {
