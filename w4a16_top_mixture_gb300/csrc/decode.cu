@@ -966,56 +966,57 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
               hsum[m] += (hv[m][j].x + hv[m][j].y) + (hv[m][j].z + hv[m][j].w);
             }
           }
-          // the expert's rows of this CTA: one ring item when they fit a stage (always, at production width)
-          const uint8_t* item0 = dn_items == 1 ? stage_at(aa) : nullptr;
-#pragma unroll 1
-          for (int rg = rlo; rg < rhi; rg += 4) {
-            float v[4];
+          // The expert's rows of this CTA are one ring item (the plan guarantees it for one token). A warp takes
+          // eight consecutive rows from rlo: rows past rhi are read (they lie inside the same stage) and
+          // dropped, so the eight dot products run unpredicated as independent chains.
+          const uint8_t* item0 = stage_at(aa);
+          float v[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              v[q] = 0.f;
-              const int rr = rg + q;
-              if (rr < rhi) {
-                const uint8_t* row = item0 ? item0 + rr * (int)L.DR
-                                           : stage_at(aa * dn_items + rr / DRPI) + (size_t)(rr % DRPI) * L.DR;
-                if (!ctl->abort)
+          for (int q = 0; q < 8; ++q) {
+            v[q] = 0.f;
+            const uint8_t* row = item0 + (rlo + q) * (int)L.DR;
 #pragma unroll
-                  for (int m = 0; m < NCL; ++m) {
-                    const int c = lane + 32 * m;
-                    if (NC % 32 == 0 || c < NC) {
-                      const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
-                      float2 qq[8];
-                      unpack_int4_quad(w.x & 0xFFFFu, qq[0], qq[1]);
-                      unpack_int4_quad(w.x >> 16, qq[2], qq[3]);
-                      unpack_int4_quad(w.y & 0xFFFFu, qq[4], qq[5]);
-                      unpack_int4_quad(w.y >> 16, qq[6], qq[7]);
-                      const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + I / 2 + (c >> 2) * 4));
-                      float2 acc = make_float2(0.f, 0.f);
+            for (int m = 0; m < NCL; ++m) {
+              const int c = lane + 32 * m;
+              if (NC % 32 == 0 || c < NC) {
+                const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+                float2 qq[8];
+                unpack_int4_quad(w.x & 0xFFFFu, qq[0], qq[1]);
+                unpack_int4_quad(w.x >> 16, qq[2], qq[3]);
+                unpack_int4_quad(w.y & 0xFFFFu, qq[4], qq[5]);
+                unpack_int4_quad(w.y >> 16, qq[6], qq[7]);
+                const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + I / 2 + (c >> 2) * 4));
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                      for (int j = 0; j < 4; ++j) {
-                        acc = __ffma2_rn(qq[2 * j], make_float2(hv[m][j].x, hv[m][j].y), acc);
-                        acc = __ffma2_rn(qq[2 * j + 1], make_float2(hv[m][j].z, hv[m][j].w), acc);
-                      }
-                      v[q] += sb.x * (acc.x + acc.y) + sb.y * hsum[m];
-                    }
-                  }
+                for (int j = 0; j < 4; ++j) {
+                  acc = __ffma2_rn(qq[2 * j], make_float2(hv[m][j].x, hv[m][j].y), acc);
+                  acc = __ffma2_rn(qq[2 * j + 1], make_float2(hv[m][j].z, hv[m][j].w), acc);
+                }
+                v[q] += sb.x * (acc.x + acc.y) + sb.y * hsum[m];
               }
             }
-            // transposed reduction of the four values over the warp: lanes with bit 4 clear keep rows 0 and 1,
-            // the others rows 2 and 3; then bit 3 picks one of the pair; then a plain butterfly over 8 lanes
-            const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0;
-            float x0 = b4 ? v[2] : v[0], x1 = b4 ? v[3] : v[1];
-            const float y0 = b4 ? v[0] : v[2], y1 = b4 ? v[1] : v[3];
-            x0 += __shfl_xor_sync(FULL, y0, 16);
-            x1 += __shfl_xor_sync(FULL, y1, 16);
-            float z = b3 ? x1 : x0;
-            z += __shfl_xor_sync(FULL, b3 ? x0 : x1, 8);
-            z += __shfl_xor_sync(FULL, z, 4);
-            z += __shfl_xor_sync(FULL, z, 2);
-            z += __shfl_xor_sync(FULL, z, 1);
-            const int idx = lane >> 3;
-            if ((lane & 7) == 0 && rg + idx < rhi) yv[(size_t)aa * nrow + rg + idx] = z;
           }
+          // transposed reduction of the eight values over the warp (9 shuffles): bit 4 of the lane keeps rows
+          // 0-3 or 4-7, bit 3 one pair of those, bit 2 one row; then a butterfly over the last two bits.
+          // Lane 4i ends with the sum for row rlo + i.
+          const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+          float x4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float keep = b4 ? v[4 + k] : v[k], give = b4 ? v[k] : v[4 + k];
+            x4[k] = keep + __shfl_xor_sync(FULL, give, 16);
+          }
+          float x2[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const float keep = b3 ? x4[2 + k] : x4[k], give = b3 ? x4[k] : x4[2 + k];
+            x2[k] = keep + __shfl_xor_sync(FULL, give, 8);
+          }
+          float z = (b2 ? x2[1] : x2[0]) + __shfl_xor_sync(FULL, b2 ? x2[0] : x2[1], 4);
+          z += __shfl_xor_sync(FULL, z, 2);
+          z += __shfl_xor_sync(FULL, z, 1);
+          const int idx = lane >> 2;
+          if ((lane & 3) == 0 && rlo + idx < rhi) yv[(size_t)aa * nrow + rlo + idx] = z;
         }
         wstamp(a, cw, 3);
 #pragma unroll 1
@@ -1136,6 +1137,8 @@ bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch
   if (NS < 4) return false;
   const int drpi = SS / (int)L.DR, dn_items = (rows + drpi - 1) / drpi;
   if (dn_items > NS / 2) return false;
+  // one token: every expert's rows are one stage, and a warp reads eight rows from the middle one on
+  if (T == 1 && ((rows + 1) / 2 + 8 > drpi || (rows + 1) / 2 > 8)) return false;
   pl.NS = NS;
   pl.SS = SS;
   pl.smem = m.ring + NS * SS;
