@@ -40,6 +40,7 @@ struct moe_block {
   uint8_t* cscratch = nullptr;
   GemmLayout G;
   ChunkScratch CS;
+  ChunkMaps maps;
 };
 
 static thread_local char g_cuda_err[256] = "";
@@ -150,6 +151,7 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
     if (e == cudaSuccess) {
       b->G = gemm_layout_carve(L, b->gstore);
       b->CS = chunk_scratch_carve(L, c.max_tokens, b->cscratch);
+      e = chunk_make_maps(L, b->CS, c.max_tokens, &b->maps);
     }
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -234,8 +236,9 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
   b->last_T = T;
   if (T > DEC_TMAX && b->chunk) {
     int n = 0;
-    cudaError_t e = chunk_forward(b->L, b->G, b->CS, b->num_sms, x, out, T, gamma, eps, b->rec_ids, b->rec_w,
-                                  b->rec_sg, b->status, b->timeout_ns, st, &n);
+    cudaError_t e = chunk_forward(b->L, b->G, b->CS, b->maps, b->cfg.max_tokens, b->num_sms, x, out, T, gamma, eps,
+                                  b->rec_ids, b->rec_w,
+                                  b->rec_sg, b->status, b->timeout_ns, b->trace, st, &n);
     b->last_launches = n;
     if (e != cudaSuccess) return cuda_fail(e, "chunk forward");
     return MOE_OK;

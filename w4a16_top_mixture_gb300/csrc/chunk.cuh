@@ -1,17 +1,27 @@
 // Prompt-chunk path (T > 16 tokens): grouped GEMMs on the tcgen05 tensor cores.
 //
 // Weights for this path live in a second, GEMM-friendly copy ("GEMM layout"), built at load time for handles
-// whose max_tokens exceeds the decode kernel's limit:
-//   gr    router      int8 [Mr][H]  rows 0..E (E+1..Mr-1 zero), Mr = E+1 rounded up to 128
-//   gsgu  shared g/u  int8 [2Is][H] rows tile-interleaved: 128-row tile m = gate units 64m..64m+63, then up units
-//   gsdn  shared down int8 [H][Is]
-//   gegu  expert g/u  int4 [E][2I][H/2] tile-interleaved like gsgu, codes two per byte (canonical packing)
-//   gedn  expert down int4 [E][H][I/2]
-// Every int8 row has its bytes permuted inside each 8-byte block as columns 0 1 4 5 2 3 6 7, so that int8 and
-// int4 rows both yield the column pairs (k, 4+k) of an 8-column block; activations are stored in the matching
-// order (0 4 1 5 2 6 3 7 per 8 columns, "P8"), which leaves every dot product unchanged. The (s, b) pairs of each
-// matrix are stored group-major: sb[g][row] (one 32-bit fp16 pair), so a K-tile of 128 rows is one 512-byte run.
+// whose max_tokens exceeds the decode kernel's limit. Every matrix (rows = output units, columns = the
+// reduction dimension) is cut into 128-row x 64-column tiles, one quantisation group wide; the tiles of a
+// 128-row band are stored one after the other, and one tile is a single contiguous block:
+//   codes  128 rows x 64 codes   int4: 32 bytes a row (canonical packing), int8: 64 bytes a row (P8 bytes)
+//   pairs  128 (s, b) fp16 pairs, one 32-bit word a row
+// so a K-tile of a band is one bulk copy (4608 bytes int4, 8704 bytes int8). Matrices:
+//   router       int8  Mr x H    rows 0..E (E+1..Mr-1 zero), Mr = E+1 rounded up to 128
+//   shared g/u   int8  2Is x H   band m = gate units 64m..64m+63, then the matching up units
+//   shared down  int8  H x Is
+//   expert g/u   int4  E x 2I x H, banded like the shared gate/up
+//   expert down  int4  E x H x I
+// Int8 rows have the bytes of each 8-byte block in the order 0 1 4 5 2 3 6 7 so that int8 and int4 rows both
+// yield the column pairs (k, 4+k) of an 8-column block; activations are stored in the matching order
+// (0 4 1 5 2 6 3 7 per 8 columns, "P8"), which leaves every dot product unchanged.
+//
+// The GEMM multiplies the exact integer codes (as fp16) by the activations on the tensor cores, one K-tile
+// (one group) at a time into a fresh accumulator, and folds each K-tile in fp32: acc += s * D + b * sum(x),
+// with sum(x) the activations' sum over the tile's 64 columns. Activation tiles arrive by TMA tensor loads
+// (128-byte swizzled, the layout the MMA reads) through tensor maps made once per handle.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,20 +30,24 @@
 
 namespace moe {
 
+constexpr int GEMM_BLK4 = 128 * 32 + 128 * 4;   // bytes of an int4 tile
+constexpr int GEMM_BLK8 = 128 * 64 + 128 * 4;   // bytes of an int8 tile
+
 struct GemmLayout {
   int H, E, K, I, Is, Mr;
-  uint8_t *gr, *gsgu, *gsdn, *gegu, *gedn;       // codes
-  uint32_t *grs, *gsgus, *gsdns, *gegus, *gedns;  // (s, b) pairs, group-major
-  size_t gegu_expert, gedn_expert, gegus_expert, gedns_expert;   // per-expert strides (bytes / pairs)
+  uint8_t *gr, *gsgu, *gsdn, *gegu, *gedn;   // tile blocks, band-major then K-tile
+  size_t gegu_expert, gedn_expert;           // bytes per expert
 };
 
-// byte sizes of the GEMM-layout store (codes + pairs) for a block shape
+// byte size of the GEMM-layout store for a block shape
 size_t gemm_store_bytes(const MoeLayout& L);
 // carve a GEMM layout out of `base` (gemm_store_bytes bytes, 256-byte aligned)
 GemmLayout gemm_layout_carve(const MoeLayout& L, uint8_t* base);
 cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, cudaStream_t st);
 
-// scratch of the chunk path for up to Tm tokens
+constexpr int CHUNK_NT = 64;   // tokens (rows of activations) per GEMM tile
+
+// scratch of the chunk path for up to Tm tokens. Activation sums are stored K-tile-major: sum[kt][row].
 struct ChunkScratch {
   uint16_t* xp;        // [Tm][H] fp16, P8 order (block input, after RMSNorm in residual mode)
   float* logits;       // [Tm][E+1]
@@ -50,16 +64,39 @@ struct ChunkScratch {
   uint16_t* hh;        // [Tm*K][I] fp16 P8, routed h (high half)
   uint16_t* hh_lo;     // [Tm*K][I] fp16 P8, routed h (low half, scaled by 4096)
   float* y;            // [Tm*K][H] routed expert outputs (unweighted)
-  int4* groups;        // [E + Tm*K/256 + 1] (expert, first sorted row, rows) per 256-row tile group
-  int32_t* ctl;        // [16] counters: job counters, group count
+  int4* groups;        // [E + Tm*K/CHUNK_NT + 1] (expert, first sorted row, rows) per row tile
+  int32_t* ctl;        // [16] group count
 };
 size_t chunk_scratch_bytes(const MoeLayout& L, int Tm);
 ChunkScratch chunk_scratch_carve(const MoeLayout& L, int Tm, uint8_t* base);
 
+// TMA tensor maps of the GEMMs' activation operands: [buffer][box], boxes of 64 columns x 16 or 64 rows,
+// 128-byte swizzle, rows past the buffer read as zero
+enum : int { CM_XP = 0, CM_XS, CM_HS, CM_HSLO, CM_HH, CM_HHLO, CM_COUNT };
+struct ChunkMaps {
+  CUtensorMap m[CM_COUNT][2];
+};
+cudaError_t chunk_make_maps(const MoeLayout& L, const ChunkScratch& S, int Tm, ChunkMaps* out);
+
+// GEMM launch of one phase: 1 router + shared gate/up, 2 expert gate/up + shared down, 3 expert down
+struct GemmArgs {
+  GemmLayout G;
+  ChunkScratch S;
+  int T;             // tokens
+  int Tm;            // row capacity of the per-token arrays (sum strides)
+  int phase;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  uint64_t* trace;   // optional: CTA 0's SM-clock stamps of its first 64 K-tiles, [role event][64]
+  ChunkMaps maps;
+};
+cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st);
+
 // out[T][H] = block(x) (or h + block(RMSNorm(h)) when gamma != NULL) for T tokens, T <= Tm
-cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkScratch& S, int num_sms,
+cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkScratch& S, const ChunkMaps& maps,
+                          int Tm, int num_sms,
                           const uint16_t* x, uint16_t* out, int T, const uint16_t* gamma, float eps,
                           int32_t* rec_ids, float* rec_w, float* rec_sg, uint32_t* status, uint64_t timeout_ns,
-                          cudaStream_t st, int* launches);
+                          uint64_t* trace, cudaStream_t st, int* launches);
 
 }  // namespace moe
