@@ -350,7 +350,7 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   if (e != cudaSuccess) return e;
   k_chunk_prologue<<<(T + 7) / 8, 256, 0, st>>>(x, gamma, eps, T, H, S.xp);
   ++n;
-  GemmArgs ga{G, S, T, Tm, 1, status, timeout_ns, trace, maps};
+  GemmArgs ga{G, S, T, Tm, 1, status, timeout_ns, nullptr, maps};
   e = chunk_gemm_launch(ga, num_sms, st);
   if (e != cudaSuccess) return e;
   ++n;
@@ -362,11 +362,12 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   k_chunk_gather<<<(T * K + 7) / 8, 256, 0, st>>>(S.xp, S.tok_of, T * K, H, S.xs);
   ++n;
   ga.phase = 2;
-  ga.trace = nullptr;   // the trace holds the first GEMM launch
+  ga.trace = trace;     // the trace holds the expert gate/up launch
   e = chunk_gemm_launch(ga, num_sms, st);
   if (e != cudaSuccess) return e;
   ++n;
   ga.phase = 3;
+  ga.trace = nullptr;
   e = chunk_gemm_launch(ga, num_sms, st);
   if (e != cudaSuccess) return e;
   ++n;

@@ -213,10 +213,10 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         const int s = gk % NSG, ab = gk % DEPTH;
         // a_ready implies that the fold of K-tile gk - DEPTH released accumulator ab (the dequantisation
         // waited for it before filling the side buffer)
-        if (!wait(&bar->a_ready[ab], (gk / DEPTH) & 1u) || !wait(&bar->full[s], (gk / NSG) & 1u)) {
-          run = false;
-          break;
-        }
+        if (!wait(&bar->a_ready[ab], (gk / DEPTH) & 1u)) { run = false; break; }
+        if (lane == 0) GSTAMP(6, gk);
+        if (!wait(&bar->full[s], (gk / NSG) & 1u)) { run = false; break; }
+        if (lane == 0) GSTAMP(7, gk);
         if (lane == 0) {
           tc_fence_after();
           uint8_t* st = smem + s * ST_BYTES;
