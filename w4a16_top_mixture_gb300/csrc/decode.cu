@@ -84,14 +84,14 @@ struct Ctl {
 constexpr int CTL_BYTES = (sizeof(Ctl) + 127) & ~127;
 
 struct Smem {   // byte offsets of the dynamic shared-memory regions
-  int xh, xs, hss, hst, hsm, yv, shs, ring;
+  int xh, xs, hss, hst, yv, shs, ring;
 };
 
 // xh: x as fp16 [T][P][4 blocks][LW lanes] uint4 (the 8 columns of a block in pair order 0 4 1 5 2 6 3 7);
 // xs: per (token, 32-column chunk) the sums of x over the chunk's "low" and "high" pair columns;
-// hss: 16-column sums of the shared expert's hs; hst: phase C's hs [T][Is], then phase B2's staged routed h
-// (hp vectors of I floats, each in the lane order of the down dot); hsm: 16-column sums of the staged h;
-// yv: routed down results [pair][row]; shs: shared down results [token][row]; ring: the weight stages.
+// hss: 16-column sums of the shared expert's hs; hst: phase C's hs [T][Is], then (one token) the routed h
+// of the K pairs, bulk-copied in the lane order of the down dot; yv: routed down results [pair][row];
+// shs: shared down results [token][row]; ring: the weight stages.
 template <class LT>
 __host__ __device__ inline Smem smem_map(const LT& L, int T, int grid, int hp) {
   Smem m;
@@ -105,7 +105,6 @@ __host__ __device__ inline Smem smem_map(const LT& L, int T, int grid, int hp) {
     const int f = hp * L.I > T * L.Is ? hp * L.I : T * L.Is;
     o += (f * 4 + 127) & ~127;
   }
-  m.hsm = o;  o += (hp * (L.I / 16) * 4 + 127) & ~127;
   m.yv = o;   o += (T * L.K * rows * 4 + 127) & ~127;
   m.shs = o;  o += (T * rows * 4 + 127) & ~127;
   m.ring = o;
@@ -239,50 +238,6 @@ __device__ __noinline__ DotR<NR, TK> dot_rows(const uint8_t* r0, const uint8_t* 
   return out;
 }
 
-// Routed down projection of one output row against the staged h of up to NP pairs (all tokens of one expert
-// in a batch). The row is I int4 codes in canonical packing followed by I/64 (s, b) pairs; lane l covers the
-// 16-column chunks c = l + 32 m. The staged h of a pair is stored as float4 [4][I/16] (element (j, c) holds
-// columns 16c + 4j .. 16c + 4j + 3), so the lanes of a warp read consecutive 16 bytes; hsm holds the 16-column
-// sums of h. Codes are unpacked once and reused for every pair: y[p] = sum_g s_g * sum(q h) + b_g * sum(h),
-// warp-reduced (every lane receives every y[p]).
-template <int I, int NP>
-__device__ __forceinline__ void dot_down(const uint8_t* __restrict__ row, const float4* __restrict__ hst,
-                                         const float* __restrict__ hsm, int p0, int np, float (&y)[NP]) {
-  constexpr int NC = I / 16;
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int q = 0; q < NP; ++q) y[q] = 0.f;
-#pragma unroll
-  for (int c0 = 0; c0 < NC; c0 += 32) {
-    const int c = c0 + lane;
-    if (NC % 32 == 0 || c < NC) {
-      const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
-      float2 q[8];
-      unpack_int4_quad(w.x & 0xFFFFu, q[0], q[1]);
-      unpack_int4_quad(w.x >> 16, q[2], q[3]);
-      unpack_int4_quad(w.y & 0xFFFFu, q[4], q[5]);
-      unpack_int4_quad(w.y >> 16, q[6], q[7]);
-      const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + I / 2 + (c >> 2) * 4));
-#pragma unroll
-      for (int pp = 0; pp < NP; ++pp) {
-        if (pp < np) {
-          const float4* hv = hst + (size_t)(p0 + pp) * (4 * NC) + c;
-          float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 h4 = hv[j * NC];
-            acc = __ffma2_rn(q[2 * j], make_float2(h4.x, h4.y), acc);
-            acc = __ffma2_rn(q[2 * j + 1], make_float2(h4.z, h4.w), acc);
-          }
-          y[pp] += sb.x * (acc.x + acc.y) + sb.y * hsm[(p0 + pp) * NC + c];
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int pp = 0; pp < NP; ++pp) y[pp] = warp_sum(y[pp]);
-}
-
 // Top-k of one token's expert logits held by a warp. Lane l holds experts l*EPL .. l*EPL+EPL-1 (a lower lane
 // means lower indices) as order-preserving integer keys. Each of the k rounds takes the warp maximum of the lane
 // maxima (the lowest lane winning ties; within a lane the lowest index), and only the winning lane recomputes
@@ -353,7 +308,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
   float* hss = reinterpret_cast<float*>(smem + sm.hss);
   float* hst = reinterpret_cast<float*>(smem + sm.hst);
   float4* hst4 = reinterpret_cast<float4*>(smem + sm.hst);
-  float* hsm = reinterpret_cast<float*>(smem + sm.hsm);
   float* yv = reinterpret_cast<float*>(smem + sm.yv);
   float* shs = reinterpret_cast<float*>(smem + sm.shs);
   uint8_t* ring = smem + sm.ring;
@@ -626,25 +580,33 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       if (rtid == 0) stamp(a, 3);
       named_bar(BAR_R, NT);
       // this CTA's share of the routed units: segments of (active expert, unit range); then release the producer
+      // The split is by work, not by units: active expert aa with n tokens weighs n per unit, so unit u of it
+      // starts at work offset I * act_pb[aa] + u * n, and a CTA takes the units that start inside its slice of
+      // the I * pairs total. With one token this is the plain split of the U * I units.
       auto plan = [&]() {
-        const int U = ctl->U, N = U * I;
-        const int lo = range_lo(N, cta, G), hi = range_lo(N, cta + 1, G);
+        const int U = ctl->U, W = I * (int)ctl->act_pb[U];
+        const int lo = range_lo(W, cta, G), hi = range_lo(W, cta + 1, G);
         int nseg = 0;
 #pragma unroll 1
-        for (int aa = lo / I; aa * I < hi && lo < hi; ++aa) {
+        for (int aa = 0; aa < U && lo < hi; ++aa) {
+          const int w0 = I * (int)ctl->act_pb[aa], n = (int)ctl->act_pb[aa + 1] - (int)ctl->act_pb[aa];
+          if (w0 >= hi) break;
+          if (w0 + I * n <= lo) continue;
+          const int u0 = max(0, (lo - w0 + n - 1) / n), u1 = min(I, (hi - w0 + n - 1) / n);
+          if (u0 >= u1) continue;
           if (nseg == DEC_MAXSEG) { set_error(a, ctl, ERR_SEGMENTS); break; }
           ctl->seg_a[nseg] = aa;
-          ctl->seg_u0[nseg] = max(lo, aa * I) - aa * I;
-          ctl->seg_u1[nseg] = min(hi, (aa + 1) * I) - aa * I;
+          ctl->seg_u0[nseg] = u0;
+          ctl->seg_u1[nseg] = u1;
           ++nseg;
         }
         ctl->nseg = ctl->abort ? 0 : nseg;
         mbar_arrive(&ctl->route_ready);
         stamp(a, 5);
       };
-      // one token: every copy is issued right after routing and the ring holds them all, so an L2 prefetch
-      // would only queue ahead of them; with more tokens the ring wraps and the prefetch warms L2
-      const uint8_t* pf_gu = ONE ? nullptr : a.ex_gu;
+      // No L2 prefetch: its copy-engine requests (two per selected expert and token) queue ahead of, and
+      // delay, the weight copies the producer issues right after routing.
+      const uint8_t* pf_gu = nullptr;
       const size_t dn0 = (size_t)r0 * L.DR, dn1 = (size_t)r1 * L.DR;
       if (ONE) {
         // one token: the K experts in selection order are the active experts, one pair each
@@ -924,15 +886,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
     // ---- every CTA's routed h is in global memory
     if (ctid == 0 && !ctl->abort && !spin_geq(&a.counters[2], (uint32_t)G, a.timeout_ns)) set_error(a, ctl, ERR_WAIT_H);
     if (ctid == 0) stamp(a, 11);
+    named_bar(BAR_C, CT);   // thread 0's wait for every CTA's h precedes every read of it
 
-    // ---- B2: routed down projection of this CTA's rows. Active experts go in batches whose pairs fit the h
-    // stage and whose items fit half the ring; a batch's items are all held at once and its (expert, row) dots
-    // are spread over the warps.
+    // ---- B2: routed down projection of this CTA's rows
     {
       const int U = ctl->U;
-      const int lim = max(1, NS / dn_items);
-      constexpr int NPC = ONE ? 1 : 4;
-      int aa0 = 0;
       if (ONE) {
         // One token, U = K experts with one pair each, all their down items in the ring. Thread 0, which has
         // just seen every CTA's h, copies all U h vectors (already in the dot's lane order) into shared memory
@@ -1021,55 +979,96 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
         wstamp(a, cw, 3);
 #pragma unroll 1
         for (int i = 0; i < U * dn_items; ++i) release();
-        aa0 = U;
       }
+      if (!ONE) {
+        // More tokens: every warp walks the active experts' down items in ring order. An expert's work is cut
+        // into units of (half of this CTA's rows) x (up to PC of its token pairs), dealt round-robin to the
+        // warps; a unit brings its pairs' h (lane-ordered rows of I floats) from L2 into registers and runs
+        // eight rows as independent dot chains, one transposed reduction per pair.
+        constexpr int PC = 2;
+        constexpr int NCL = (NC + 31) / 32;
+        const int half = (nrow + 1) / 2;
+        int ui = 0;
 #pragma unroll 1
-      while (aa0 < U) {
-        const int pb0 = ctl->act_pb[aa0];
-        int aa1 = aa0 + 1;
+        for (int aa = 0; aa < U; ++aa) {
+          const int pb = ctl->act_pb[aa], na = (int)ctl->act_pb[aa + 1] - pb;
+          const int nunits = 2 * ((na + PC - 1) / PC);
+          const uint8_t* item = acquire();
 #pragma unroll 1
-        while (aa1 < U && aa1 - aa0 < lim && ctl->act_pb[aa1 + 1] - pb0 <= hp) ++aa1;
-        const int np = ctl->act_pb[aa1] - pb0;
-        named_bar(BAR_C, CT);   // phase C and the previous batch no longer read the stage
-        if (!ctl->abort)
-#pragma unroll 1
-          for (int i = ctid; i < np * NC; i += CT) {
-            const int p = i / NC, c = i % NC;
-            const float4* src = reinterpret_cast<const float4*>(a.hbuf + (size_t)(pb0 + p) * I);
-            float s = 0.f;
+          for (int k = 0; k < nunits; ++k, ++ui) {
+            if (ui % NCW != cw || ctl->abort) continue;
+            const int rlo = (k & 1) ? half : 0, rhi = (k & 1) ? nrow : half;
+            const int p0 = pb + (k >> 1) * PC, np = min(PC, pb + na - p0);
+            float4 hv[PC][NCL][4];
+            float hsum[PC][NCL];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float4 v = __ldcg(src + j * NC + c);
-              hst4[(size_t)p * 4 * NC + j * NC + c] = v;
-              s += (v.x + v.y) + (v.z + v.w);
-            }
-            hsm[p * NC + c] = s;
-          }
-        named_bar(BAR_C, CT);
-        if (aa0 == 0) wstamp(a, cw, 2);
-        const int nit = (aa1 - aa0) * dn_items, nwork = (aa1 - aa0) * nrow;
-#pragma unroll 1
-        for (int wu = cw; wu < nwork; wu += NCW) {
-          const int ai = wu / nrow, rr = wu % nrow;
-          const uint8_t* st = stage_at(ai * dn_items + rr / DRPI);
-          if (!ctl->abort) {
-            const uint8_t* rowp = st + (size_t)(rr % DRPI) * L.DR;
-            const int pa = ctl->act_pb[aa0 + ai] - pb0, na = ctl->act_pb[aa0 + ai + 1] - pb0 - pa;
-#pragma unroll 1
-            for (int pc = 0; pc < na; pc += NPC) {
-              float y[NPC];
-              dot_down<I, NPC>(rowp, hst4, hsm, pa + pc, min(NPC, na - pc), y);
-              if (lane == 0)
+            for (int pp = 0; pp < PC; ++pp)
 #pragma unroll
-                for (int pp = 0; pp < NPC; ++pp)
-                  if (pp < na - pc) yv[(size_t)(pb0 + pa + pc + pp) * nrow + rr] = y[pp];
+              for (int m = 0; m < NCL; ++m) {
+                const int c = lane + 32 * m;
+                hsum[pp][m] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  hv[pp][m][j] = (pp < np && (NC % 32 == 0 || c < NC))
+                                     ? __ldcg(reinterpret_cast<const float4*>(a.hbuf + (size_t)(p0 + pp) * I) + j * NC + c)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                  hsum[pp][m] += (hv[pp][m][j].x + hv[pp][m][j].y) + (hv[pp][m][j].z + hv[pp][m][j].w);
+                }
+              }
+            float v[PC][8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+#pragma unroll
+              for (int pp = 0; pp < PC; ++pp) v[pp][q] = 0.f;
+              const uint8_t* row = item + (rlo + q) * (int)L.DR;
+#pragma unroll
+              for (int m = 0; m < NCL; ++m) {
+                const int c = lane + 32 * m;
+                if (NC % 32 == 0 || c < NC) {
+                  const uint2 w = *reinterpret_cast<const uint2*>(row + c * 8);
+                  float2 qq[8];
+                  unpack_int4_quad(w.x & 0xFFFFu, qq[0], qq[1]);
+                  unpack_int4_quad(w.x >> 16, qq[2], qq[3]);
+                  unpack_int4_quad(w.y & 0xFFFFu, qq[4], qq[5]);
+                  unpack_int4_quad(w.y >> 16, qq[6], qq[7]);
+                  const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + I / 2 + (c >> 2) * 4));
+#pragma unroll
+                  for (int pp = 0; pp < PC; ++pp) {
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                      acc = __ffma2_rn(qq[2 * j], make_float2(hv[pp][m][j].x, hv[pp][m][j].y), acc);
+                      acc = __ffma2_rn(qq[2 * j + 1], make_float2(hv[pp][m][j].z, hv[pp][m][j].w), acc);
+                    }
+                    v[pp][q] += sb.x * (acc.x + acc.y) + sb.y * hsum[pp][m];
+                  }
+                }
+              }
+            }
+            const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+            const int idx = lane >> 2;
+#pragma unroll
+            for (int pp = 0; pp < PC; ++pp) {
+              float x4[4];
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const float keep = b4 ? v[pp][4 + kk] : v[pp][kk], give = b4 ? v[pp][kk] : v[pp][4 + kk];
+                x4[kk] = keep + __shfl_xor_sync(FULL, give, 16);
+              }
+              float x2[2];
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                const float keep = b3 ? x4[2 + kk] : x4[kk], give = b3 ? x4[kk] : x4[2 + kk];
+                x2[kk] = keep + __shfl_xor_sync(FULL, give, 8);
+              }
+              float z = (b2 ? x2[1] : x2[0]) + __shfl_xor_sync(FULL, b2 ? x2[0] : x2[1], 4);
+              z += __shfl_xor_sync(FULL, z, 2);
+              z += __shfl_xor_sync(FULL, z, 1);
+              if ((lane & 3) == 0 && pp < np && rlo + idx < rhi) yv[(size_t)(p0 + pp) * nrow + rlo + idx] = z;
             }
           }
+          release();
         }
-        if (aa0 == 0) wstamp(a, cw, 3);
-#pragma unroll 1
-        for (int i = 0; i < nit; ++i) release();
-        aa0 = aa1;
       }
     }
     named_bar(BAR_C, CT);
@@ -1123,7 +1122,7 @@ bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch
   if (rows > DEC_MAXROWS) return false;
   DecodeLaunch pl;
   pl.grid = grid;
-  pl.hp = T == 1 ? L.K : DEC_HP;
+  pl.hp = T == 1 ? L.K : 0;   // h vectors staged in shared memory (one token only)
   const Smem m = smem_map(L, T, grid, pl.hp);
   int SS = (int)(4 * L.EU);
   if (SS < 4 * L.H) SS = 4 * L.H;
@@ -1137,8 +1136,8 @@ bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch
   if (NS < 4) return false;
   const int drpi = SS / (int)L.DR, dn_items = (rows + drpi - 1) / drpi;
   if (dn_items > NS / 2) return false;
-  // one token: every expert's rows are one stage, and a warp reads eight rows from the middle one on
-  if (T == 1 && ((rows + 1) / 2 + 8 > drpi || (rows + 1) / 2 > 8)) return false;
+  // every expert's rows are one stage, and a warp reads eight rows from the middle one on
+  if ((rows + 1) / 2 + 8 > drpi || (rows + 1) / 2 > 8) return false;
   pl.NS = NS;
   pl.SS = SS;
   pl.smem = m.ring + NS * SS;

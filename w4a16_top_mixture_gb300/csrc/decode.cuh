@@ -11,7 +11,6 @@ constexpr int DEC_THREADS = (DEC_NCW + 1) * 32;   // + one producer warp
 constexpr int DEC_TMAX = 16;                      // largest T of the fused decode kernel
 constexpr int DEC_MAXSEG = 4;                     // expert segments one CTA's unit range may touch
 constexpr int DEC_MAXROWS = 32;                   // output rows one CTA owns (ceil(H / grid))
-constexpr int DEC_HP = 16;                        // routed h vectors staged in shared memory at once (T > 1)
 constexpr int DEC_MAXNS = 24;                     // ring stages
 constexpr int DEC_MAXGRID = 160;                  // CTAs (one per SM)
 
@@ -42,7 +41,7 @@ struct DecodeArgs {
 };
 
 struct DecodeLaunch {
-  int grid, smem, NS, SS, hp;   // hp: routed h vectors the shared-memory stage holds
+  int grid, smem, NS, SS, hp;   // hp: routed h vectors staged in shared memory (one token: K; else 0)
 };
 
 // Host: shared-memory plan for a call with T tokens; returns false if it does not fit.
