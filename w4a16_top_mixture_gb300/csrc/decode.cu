@@ -856,6 +856,19 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
 #pragma unroll 1
             for (int tc = 0; tc < ne; tc += TK) {
               const int nt = min(TK, ne - tc);
+              if (TK > 1 && nt == 1) {
+                // a lone token (most experts at small batch under top-k routing): the single-token dot, not the
+                // token-pair one with half of its products on a zero activation
+                const DotR<4, 1> d1 = dot_rows<H, 4, 1, false>(ub, ub + H / 2, ub + L.EU, ub + L.EU + H / 2,
+                                                               ub + H, ub + H + L.GB * 4, ub + L.EU + H,
+                                                               ub + L.EU + H + L.GB * 4, nvalid, xh, xs, toks[tc],
+                                                               toks[tc], 1);
+                if (lane < 2) {
+                  const float g = lane ? d1.v[0][2] : d1.v[0][0], up = lane ? d1.v[0][3] : d1.v[0][1];
+                  if (2 * lane < nvalid) hrow[(size_t)tc * I + hpos<I>(ui + lane)] = silu_fast(g) * up;
+                }
+                continue;
+              }
               const DotR<4, TK> d = dot_rows<H, 4, TK, false>(ub, ub + H / 2, ub + L.EU, ub + L.EU + H / 2,
                                                               ub + H, ub + H + L.GB * 4, ub + L.EU + H,
                                                               ub + L.EU + H + L.GB * 4, nvalid, xh, xs, toks[tc],
@@ -1124,7 +1137,9 @@ bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch
   pl.grid = grid;
   pl.hp = T == 1 ? L.K : 0;   // h vectors staged in shared memory (one token only)
   const Smem m = smem_map(L, T, grid, pl.hp);
-  int SS = (int)(4 * L.EU);
+  // one token: 4 gate/up units a stage keeps every item of the call in the ring at once; more tokens: the ring
+  // wraps anyway, and 8 units (4 unit pairs, 4 warps) a stage put more warps to work on each landed item
+  int SS = (int)((T == 1 ? 4 : 8) * L.EU);
   if (SS < 4 * L.H) SS = 4 * L.H;
   if ((int)(2 * L.SU) > SS) SS = (int)(2 * L.SU);
   if ((int)L.RR > SS) SS = (int)L.RR;
