@@ -198,6 +198,103 @@ print(json.dumps({{"tokens": n, "seconds": time.perf_counter() - t0}}))
     print(json.dumps(line), flush=True)
 
 
+def _time_graph(fn, reps=10, per=20):
+    """Device time per call of fn (CUDA events around replays of a graph of `per` calls), after warm-up."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(per):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * per)
+
+
+def extra_configs(blocks, X):
+    """Throughput of the other block configurations (tokens/s and us per block), each on synthetic inputs of its
+    shape; inputs are device-resident, times are device times of graph-replayed calls."""
+    import torch
+    from w4a16_top_mixture_gb300 import lib
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _cases import make_case   # seeded inputs that respect the routing-gap rule (generators only)
+    out = {}
+
+    def dev(x):
+        return torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
+
+    # tiny block, T = 1
+    w, x = make_case(synth.TINY, 1, 5)
+    b = lib.MoeBlock.from_config(synth.TINY, max_tokens=1)
+    b.load_weights(w)
+    xd, od = dev(x), torch.empty((1, synth.TINY.hidden), dtype=torch.float16, device="cuda")
+    us = _time_graph(lambda: b.forward(xd, od))
+    out["tiny_T1"] = {"us_per_block": us, "tokens_per_s": 1e6 / us, "note": "L2-resident (one tiny layer)"}
+    b.close()
+    # production block, T = 16, Zipf(1.1) routing, 4 layers rotated
+    cfg = synth.PROD
+    bs, xs = [], []
+    for l in range(4):
+        w, x = make_case(cfg, 16, 42 + l, routing="zipf")
+        b = lib.MoeBlock.from_config(cfg, max_tokens=16)
+        b.load_weights(w)
+        bs.append(b)
+        xs.append(dev(x))
+    od = torch.empty((16, cfg.hidden), dtype=torch.float16, device="cuda")
+    it = [0]
+
+    def step16():
+        i = it[0] % 4
+        it[0] += 1
+        bs[i].forward(xs[i], od)
+    us = _time_graph(step16)
+    out["batched_T16_zipf"] = {"us_per_block": us, "tokens_per_s": 16e6 / us}
+    for b in bs:
+        b.close()
+    # 40 stacked layers with RMSNorm + residual, T = 1: one token through every layer per call
+    h = [X[0:1].clone(), torch.empty_like(X[0:1])]
+
+    def stack():
+        for l, b in enumerate(blocks):
+            b.forward_residual(h[l & 1], h[(l + 1) & 1])
+    us = _time_graph(stack, reps=5, per=5)
+    out["stack_T1"] = {"layers": len(blocks), "us_per_token": us, "us_per_block": us / len(blocks),
+                       "tokens_per_s": 1e6 / us}
+    # prompt chunk T = 512, uniform and Zipf routing (tcgen05 grouped-GEMM path)
+    for routing, seed in (("uniform", 553), ("zipf", 42)):
+        w, x = make_case(cfg, 512, seed, routing=routing)
+        b = lib.MoeBlock.from_config(cfg, max_tokens=512)
+        b.load_weights(w)
+        xd, od = dev(x), torch.empty((512, cfg.hidden), dtype=torch.float16, device="cuda")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        ts = []
+        for r in range(13):
+            flush.fill_(r)            # the layer's 0.9 GB of weights exceed L2 anyway; the flush makes sure
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            b.forward(xd, od)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        us = float(np.median(ts))
+        out[f"chunk_T512_{routing}"] = {"us_per_block": us, "tokens_per_s": 512e6 / us}
+        b.close()
+        del flush
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -214,7 +311,7 @@ def run_ours(args):
     NL = args.layers
     blocks = []
     for l in range(NL):
-        w = synth.gen_layer(cfg, rank_seed(rank), l)
+        w = synth.gen_layer(cfg, rank_seed(rank), l, with_gamma=True)   # gamma serves the stack config
         b = lib.MoeBlock.from_config(cfg, max_tokens=1)
         b.load_weights(w)                      # host arrays: copied and repacked by the library
         blocks.append(b)
@@ -320,6 +417,8 @@ def run_ours(args):
             "gpu_launches": launches,
             "clocks": clk.summary(),
         }
+        if not args.no_extras:
+            line["configs"] = extra_configs(blocks, X)
         print(json.dumps(line), flush=True)
     for b in blocks:
         b.close()
@@ -335,6 +434,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=40)
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle leg (profiling runs)")
+    ap.add_argument("--no-extras", action="store_true", help="omit the other block configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
