@@ -78,7 +78,7 @@ struct ChunkMaps {
 };
 cudaError_t chunk_make_maps(const MoeLayout& L, const ChunkScratch& S, int Tm, ChunkMaps* out);
 
-// GEMM launch of one phase: 1 router + shared gate/up, 2 expert gate/up + shared down, 3 expert down
+// GEMM launch of one phase: 1 router + shared gate/up, 2 expert gate/up, 3 expert down + shared down
 struct GemmArgs {
   GemmLayout G;
   ChunkScratch S;

@@ -11,12 +11,24 @@
 // same jobs and K-tiles and handing stages over on mbarriers:
 //   warp 0     producer (one lane): a bulk copy of the K-tile's weight block (codes + pairs) and TMA tensor
 //              loads of the activation rows (128-byte swizzled K-major), all on the stage's "full" barrier
-//   warp 1     allocates TMEM; lane 0 issues the MMAs and commits them to the barriers that free the stage,
-//              the A buffer and hand the accumulator to the fold
-//   warps 2-9  dequantise, two groups of four warps taking alternate K-tiles: thread = band row, codes ->
-//              exact fp16 integers in the swizzled A buffer; the threads of rows 64-127 also sum activation
-//              rows 0-63 of the tile (the fold's sum(x))
+//   warps 1, 14  lane 0 issues the MMAs of the even (warp 1) or odd (warp 14) K-tiles (A from tensor memory,
+//              B from shared memory) and commits them to the stage's "empty" barrier; warp 1 also owns TMEM
+//   warps 2-9  dequantise, two groups of four warps taking alternate K-tiles: thread = band row = TMEM lane,
+//              codes -> exact fp16 integers stored straight into the slot's A columns of tensor memory; the
+//              group also sums the tile's activation rows (the fold's sum(x)), one (row, 16-byte chunk) item
+//              per thread
 //   warps 10-13 fold (thread = TMEM lane = band row) and, after the job's last K-tile, the epilogue
+// K-tile gk uses shared-memory stage gk % NSG and tensor-memory slot gk % nt (A operand, accumulator and side
+// buffer); there are more stages than slots so that more weight copies are in flight. Slots hold a low-half
+// accumulator only in phase 3 (the down projections, whose B is split into hi + lo halves), so phases 1 and 2
+// fit 5 slots into the 512 columns and phase 3 fits 3. Handoffs:
+//   full[s]    the copies landed                                     (producer -> dequantisation)
+//   a_ready[t] A and the side buffer are written                     (dequantisation -> MMA)
+//   empty[s]   the dequantisation has read the stage and the MMAs have completed: the stage is free and the
+//              accumulator holds the K-tile                          (-> producer, fold)
+//   d_free[t]  the fold has read the accumulator and the side buffer; since the fold saw empty[s], the MMAs
+//              that read A are complete too                          (fold -> dequantisation)
+// Keeping A out of shared memory leaves the shared-memory pipe to the copies, the code loads and B.
 // Every wait is bounded; on a timeout the CTA records an error bit and every role leaves its loops.
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -31,17 +43,19 @@ namespace {
 
 enum : int { GK_ROUTER = 0, GK_SHGU = 1, GK_SHDN = 2, GK_EXGU = 3, GK_EXDN = 4 };
 
-constexpr int GTH = 448;                // 14 warps
-constexpr int NSG = 4;                  // pipeline stages
-constexpr int DEPTH = 4;                // A buffers = TMEM accumulators = side buffers (K-tiles in flight
-                                        // between the dequantisation and the fold)
+constexpr int GTH = 480;                // 15 warps
+constexpr int NSG = 6;                  // shared-memory stages
+constexpr int NT_MAX = 5;               // tensor-memory slots (phases 1 and 2; phase 3: 3)
+// tensor-memory slot: accumulator hi (64 columns) | [phase 3: accumulator lo (64)] | A: 128 rows x 64 fp16
+// (32 columns)
+constexpr uint32_t TM_LO = 64;
+static_assert(5 * 96 <= 512 && 3 * 160 <= 512, "tensor memory");
 // stage layout: weight block | B hi (64 rows x 128 B, swizzled) | B lo
 constexpr int ST_W = 0, ST_BHI = 9216, ST_BLO = 17408, ST_BYTES = 25600;
-constexpr int S_A = NSG * ST_BYTES;                 // DEPTH A buffers of 128 x 64 fp16 (16 KB each)
-constexpr int S_SIDE = S_A + DEPTH * 16384;         // DEPTH side buffers: (s, b) of 128 rows, 64 row sums
+constexpr int S_SIDE = NSG * ST_BYTES;              // NT_MAX side buffers: (s, b) of 128 rows, 64 row sums
 constexpr int SIDE_BYTES = 128 * 4 + 64 * 4;
-constexpr int S_XCH = S_SIDE + DEPTH * SIDE_BYTES;  // SwiGLU exchange: up values [64][65]
-constexpr int S_BAR = S_XCH + 64 * 65 * 4;
+constexpr int S_EP = S_SIDE + NT_MAX * SIDE_BYTES;  // epilogue staging of a job's accumulator: [128][65]
+constexpr int S_BAR = S_EP + 128 * 65 * 4;
 constexpr int S_BYTES = S_BAR + 256;
 constexpr int GEMM_SMEM = S_BYTES + 1024;           // + alignment slack
 constexpr uint32_t ERR_GEMM_WAIT = 512u;
@@ -54,9 +68,19 @@ struct Job {
   int row0, cnt, n;       // first activation row, rows, MMA N (cnt rounded up to 16)
 };
 
-__device__ bool decode_job(const GemmArgs& g, int j, Job& jb) {
+// tensor-memory slot of a role's current K-tile and the parity of that slot's current use
+struct SlotRing {
+  int t = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int nt) {
+    if (++t == nt) { t = 0; ph ^= 1u; }
+  }
+};
+
+// Job j of the phase. Phases 2 and 3 take the expert row-tile count (ngroups) and job j's row-tile entry gr
+// (S.groups[j % ngroups] for the expert jobs) from the caller, which loads them ahead of time.
+__device__ __forceinline__ bool decode_job(const GemmArgs& g, int j, int ngroups, int4 gr, Job& jb) {
   const GemmLayout& G = g.G;
-  const ChunkScratch& S = g.S;
   const int H = G.H, I = G.I, Is = G.Is, T = g.T;
   const int NTT = (T + CHUNK_NT - 1) / CHUNK_NT;
   jb.e = 0;
@@ -79,14 +103,12 @@ __device__ bool decode_job(const GemmArgs& g, int j, Job& jb) {
       jb.bmap = CM_XP;
     }
   } else {
-    const int ngroups = S.ctl[0];
     const int MTg = 2 * I / 128, MTd = H / 128;
-    const int nex = (g.phase == 2 ? MTg : MTd) * ngroups;
+    const int nex = (g.phase == 2 ? MTg : MTd) * ngroups;   // expert jobs; phase 3 then the shared down
     if (j < nex) {
       // band-major: the row tiles of one expert for one band are consecutive jobs (they share the band's
       // weights through L2)
       const int m = j / ngroups;
-      const int4 gr = S.groups[j % ngroups];
       jb.m = m; jb.e = gr.x; jb.row0 = gr.y; jb.cnt = gr.z; jb.int8 = 0;
       if (g.phase == 2) {
         jb.kind = GK_EXGU;
@@ -99,7 +121,7 @@ __device__ bool decode_job(const GemmArgs& g, int j, Job& jb) {
       }
     } else {
       j -= nex;
-      if (g.phase != 2 || j >= MTd * NTT) return false;
+      if (g.phase != 3 || j >= MTd * NTT) return false;
       jb.kind = GK_SHDN; jb.m = j % MTd; token_tile(j / MTd);
       jb.w = G.gsdn + (size_t)jb.m * (Is / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = Is / 64;
       jb.bmap = CM_HS; jb.lomap = CM_HSLO;
@@ -109,8 +131,31 @@ __device__ bool decode_job(const GemmArgs& g, int j, Job& jb) {
   return jb.cnt > 0;
 }
 
+// A role's walk over its CTA's jobs j = blockIdx.x + k * gridDim.x. The row-tile entry of the next job is
+// loaded while the current one runs, so a job change costs no global-memory round trip.
+struct JobIter {
+  int j, ngroups;
+  int4 gr;
+};
+__device__ __forceinline__ int4 job_group(const GemmArgs& g, int ngroups, int j) {
+  const int MT = g.phase == 2 ? 2 * g.G.I / 128 : g.G.H / 128;
+  if (g.phase == 1 || ngroups <= 0 || j >= MT * ngroups) return make_int4(0, 0, 0, 0);
+  return g.S.groups[j % ngroups];
+}
+__device__ __forceinline__ void job_begin(const GemmArgs& g, JobIter& it) {
+  it.j = blockIdx.x;
+  it.ngroups = g.phase == 1 ? 0 : g.S.ctl[0];
+  it.gr = job_group(g, it.ngroups, it.j);
+}
+__device__ __forceinline__ bool job_next(const GemmArgs& g, JobIter& it, Job& jb) {
+  const bool ok = decode_job(g, it.j, it.ngroups, it.gr, jb);
+  it.j += gridDim.x;
+  it.gr = job_group(g, it.ngroups, it.j);
+  return ok;
+}
+
 struct Bars {
-  uint64_t full[NSG], empty[NSG], a_ready[DEPTH], a_free[DEPTH], d_full[DEPTH], d_free[DEPTH];
+  uint64_t full[NSG], empty[NSG], a_ready[NT_MAX], d_free[NT_MAX];
   uint64_t fold_sync;   // the four fold warps meet here in the SwiGLU epilogue (a bounded wait)
   uint32_t tslot;
   volatile int abort;
@@ -121,6 +166,15 @@ struct Bars {
 #define GSTAMP(ev, k) do { if (g.trace && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
 
 __device__ __forceinline__ float silu_c(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// sum of the 8 fp16 values of a 16-byte chunk, in fp32
+__device__ __forceinline__ float sum8_h(uint4 v) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+  const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
+  return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
+}
 
 // position of unit u of an h vector in P8 order
 __device__ __forceinline__ int p8u(int u) {
@@ -147,9 +201,12 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     bar->abort = 1;
   };
   // bounded wait on phase parity `ph` of `b`; false (and the CTA aborts) on a timeout or an earlier abort
+  // bounded wait on phase parity `ph` of `b`; false (and the CTA aborts) on a timeout; a wait that does not
+  // complete at once gives up straight away if the CTA has already aborted
   auto wait = [&](uint64_t* b, uint32_t ph) -> bool {
+    if (mbar_try_wait(b, ph)) return true;
     if (bar->abort) return false;
-    if (!mbar_wait(b, ph, to)) { fail(); return false; }
+    if (!mbar_wait_slow(b, ph, to)) { fail(); return false; }
     return true;
   };
 
@@ -158,10 +215,8 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       mbar_init(&bar->full[s], 1);          // the producer's expect-tx arrival
       mbar_init(&bar->empty[s], 4 + 1);     // dequant warps (codes, pairs, sums read) + MMA commit (B read)
     }
-    for (int i = 0; i < DEPTH; ++i) {
+    for (int i = 0; i < NT_MAX; ++i) {
       mbar_init(&bar->a_ready[i], 4);
-      mbar_init(&bar->a_free[i], 1);
-      mbar_init(&bar->d_full[i], 1);
       mbar_init(&bar->d_free[i], 4);
     }
     mbar_init(&bar->fold_sync, 4);
@@ -173,15 +228,20 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar->tslot;
+  // slot geometry of this phase
+  const bool lo_phase = g.phase == 3;
+  const int nt = lo_phase ? 3 : 5;
+  const uint32_t slot_cols = lo_phase ? 160u : 96u, a_col = lo_phase ? 128u : 64u;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer (lane 0)
     if (lane == 0) {
       uint32_t gk = 0;
       bool run = true;
-      for (int j = blockIdx.x; run; j += gridDim.x) {
-        Job jb;
-        if (!decode_job(g, j, jb)) break;
+      JobIter it;
+      job_begin(g, it);
+      Job jb;
+      while (run && job_next(g, it, jb)) {
         const int blk = jb.int8 ? GEMM_BLK8 : GEMM_BLK4;
         const int box = jb.n <= 16 ? 0 : 1;
         const uint32_t bbytes = (box ? CHUNK_NT : 16) * 128;
@@ -201,113 +261,106 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       for (uint32_t q = gk - cnt; q < gk; ++q) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issue
-    uint32_t gk = 0;
-    bool run = true;
-    for (int j = blockIdx.x; run; j += gridDim.x) {
+  } else if (warp == 1 || warp == 14) {
+    // ------------------------------------------------------------------ MMA issue (lane 0)
+    // Two issuing threads, alternate K-tiles: one thread's tcgen05.mma issue costs tens of cycles, and the
+    // accumulators of consecutive K-tiles are independent.
+    const uint32_t par = warp == 1 ? 0u : 1u;
+    if (lane == 0) {
+      uint32_t gk = 0;
+      bool run = true;
+      JobIter it;
+      job_begin(g, it);
       Job jb;
-      if (!decode_job(g, j, jb)) break;
-      const uint32_t idesc = umma_idesc_f16(128, jb.n);
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk) {
-        const int s = gk % NSG, ab = gk % DEPTH;
-        // a_ready implies that the fold of K-tile gk - DEPTH released accumulator ab (the dequantisation
-        // waited for it before filling the side buffer)
-        if (!wait(&bar->a_ready[ab], (gk / DEPTH) & 1u)) { run = false; break; }
-        if (lane == 0) GSTAMP(6, gk);
-        if (!wait(&bar->full[s], (gk / NSG) & 1u)) { run = false; break; }
-        if (lane == 0) GSTAMP(7, gk);
-        if (lane == 0) {
+      SlotRing sl;
+      while (run && job_next(g, it, jb)) {
+        const uint32_t idesc = umma_idesc_f16(128, jb.n);
+        const bool lo = jb.lomap >= 0;
+        for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt)) {
+          if ((gk & 1u) != par) continue;
+          const int s = gk % NSG, t = sl.t;
+          // a_ready implies full[s] and that the fold of K-tile gk - nt released slot t (the dequantisation
+          // waited for both)
+          if (!wait(&bar->a_ready[t], sl.ph)) { run = false; break; }
+          GSTAMP(6, gk);
           tc_fence_after();
-          uint8_t* st = smem + s * ST_BYTES;
-          const uint32_t a0 = smem_u32(smem + S_A + ab * 16384);
-          const uint32_t bh = smem_u32(st + ST_BHI), bl = smem_u32(st + ST_BLO);
-          const uint32_t d = tmem + ab * 128;
+          // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
+          const uint8_t* st = smem + s * ST_BYTES;
+          const uint64_t bh = umma_desc_sw128(smem_u32(st + ST_BHI)), bl = umma_desc_sw128(smem_u32(st + ST_BLO));
+          const uint32_t d = tmem + t * slot_cols, a = d + a_col;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_f16(d, umma_desc_sw128(a0 + 32 * ks), umma_desc_sw128(bh + 32 * ks), idesc, ks > 0 ? 1u : 0u);
-          if (jb.lomap >= 0)
+          for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, ks > 0 ? 1u : 0u);
+          if (lo)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_f16(d + 64, umma_desc_sw128(a0 + 32 * ks), umma_desc_sw128(bl + 32 * ks), idesc, ks > 0 ? 1u : 0u);
-          umma_commit(&bar->a_free[ab]);
-          umma_commit(&bar->d_full[ab]);
+            for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d + TM_LO, a + 8 * ks, bl + 2 * ks, idesc, ks > 0 ? 1u : 0u);
           umma_commit(&bar->empty[s]);
           GSTAMP(3, gk);
         }
-        __syncwarp();
       }
+      // this thread's last MMAs must have completed before TMEM is released
+      const uint32_t last = gk == 0 ? 0u : ((gk - 1) & 1u) == par ? gk - 1 : gk - 2;
+      if (gk > par) mbar_wait(&bar->empty[last % NSG], (last / NSG) & 1u, to);
     }
-    // the last MMAs must have completed before TMEM is released
-    if (lane == 0 && gk > 0) mbar_wait(&bar->d_full[(gk - 1) % DEPTH], ((gk - 1) / DEPTH) & 1u, to);
     __syncwarp();
   } else if (warp < 10) {
     // ------------------------------------------------------------------ dequantise
     const int grp = (warp - 2) >> 2;          // this group takes the K-tiles gk with gk % 2 == grp
-    const int r = (tid - 64) & 127;           // band row
+    const int r = (warp & 3) * 32 + lane;     // band row = the TMEM lane this warp may access
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const __half2 k1024 = __float2half2_rn(1024.0f), k16 = __float2half2_rn(0.0625f), k64 = __float2half2_rn(-64.0f);
     uint32_t gk = 0;
     bool run = true;
-    for (int j = blockIdx.x; run; j += gridDim.x) {
-      Job jb;
-      if (!decode_job(g, j, jb)) break;
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk) {
+    JobIter it;
+    job_begin(g, it);
+    Job jb;
+    SlotRing sl;
+    while (run && job_next(g, it, jb)) {
+      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt)) {
         if ((int)(gk & 1u) != grp) continue;
-        const int s = gk % NSG, ab = gk % DEPTH;
-        const uint32_t pf = ((gk / DEPTH) & 1u) ^ 1u;   // phase of K-tile gk - DEPTH
+        const int s = gk % NSG, t = sl.t;
+        // d_free[t] of K-tile gk - nt: the fold is done with slot t, and the MMAs that read its A are complete
         if (!wait(&bar->full[s], (gk / NSG) & 1u) ||
-            (gk >= DEPTH && (!wait(&bar->a_free[ab], pf) || !wait(&bar->d_free[ab], pf)))) {
+            (gk >= (uint32_t)nt && !wait(&bar->d_free[t], sl.ph ^ 1u))) {
           run = false;
           break;
         }
         if (r == 0) GSTAMP(1, gk);
         const uint8_t* st = smem + s * ST_BYTES + ST_W;
-        uint8_t* A = smem + S_A + ab * 16384;
         // the fold's share of the stage goes to the side buffer, so the stage is free once the MMA has read B
         {
-          uint32_t* side = reinterpret_cast<uint32_t*>(smem + S_SIDE + ab * SIDE_BYTES);
+          uint32_t* side = reinterpret_cast<uint32_t*>(smem + S_SIDE + t * SIDE_BYTES);
           side[r] = *reinterpret_cast<const uint32_t*>(st + 128 * (jb.int8 ? 64 : 32) + r * 4);
-          const int xr = r - 64;   // activation row summed by this thread
-          if (xr >= 0 && xr < jb.n) {
-            // sum of activation row xr over the tile's 64 columns (swizzled 16-byte chunks); low halves / 4096
-            const uint8_t* bst = smem + s * ST_BYTES;
-            float sh = 0.f, sl = 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t off = sw128_off(xr, c);
-              const uint4 v = *reinterpret_cast<const uint4*>(bst + ST_BHI + off);
-              const __half2* hv = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 f = __half22float2(hv[k]);
-                sh += f.x + f.y;
-              }
-              if (jb.lomap >= 0) {
-                const uint4 u = *reinterpret_cast<const uint4*>(bst + ST_BLO + off);
-                const __half2* hu = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const float2 f = __half22float2(hu[k]);
-                  sl += f.x + f.y;
-                }
-              }
-            }
-            reinterpret_cast<float*>(side)[128 + xr] = fmaf(sl, 1.0f / 4096.0f, sh);
+          // sums of the tile's activation rows over its 64 columns (low halves / 4096): one (row, 16-byte
+          // chunk) item per thread, the 8 chunks of a row on 8 neighbouring lanes. jb.n * 8 is a multiple of
+          // 128, so every warp of the group runs the same iterations.
+          const uint8_t* bst = smem + s * ST_BYTES;
+          float* xsum = reinterpret_cast<float*>(side) + 128;
+#pragma unroll 1
+          for (int i = r; i < jb.n * 8; i += 128) {
+            const int row = i >> 3, c = i & 7;
+            const uint32_t off = sw128_off(row, c);
+            float tot = sum8_h(*reinterpret_cast<const uint4*>(bst + ST_BHI + off));
+            if (jb.lomap >= 0) tot = fmaf(sum8_h(*reinterpret_cast<const uint4*>(bst + ST_BLO + off)), 1.0f / 4096.0f, tot);
+            tot += __shfl_xor_sync(0xFFFFFFFFu, tot, 1);
+            tot += __shfl_xor_sync(0xFFFFFFFFu, tot, 2);
+            tot += __shfl_xor_sync(0xFFFFFFFFu, tot, 4);
+            if (c == 0) xsum[row] = tot;
           }
         }
+        // row r of A in K order: column 4c + k of the slot holds the fp16 pair k of 8-column block c
+        uint32_t arow[32];
         if (jb.int8) {
           const uint8_t* codes = st + r * 64;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint2 w = *reinterpret_cast<const uint2*>(codes + c * 8);
-            uint32_t v[4], o[4];
+            uint32_t v[4];
             int8_block_pairs(w.x, w.y, v);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&v[k]), k1024);
-              o[k] = *reinterpret_cast<const uint32_t*>(&q);
+              arow[4 * c + k] = *reinterpret_cast<const uint32_t*>(&q);
             }
-            *reinterpret_cast<uint4*>(A + sw128_off(r, c)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         } else {
           const uint8_t* codes = st + r * 32;
@@ -315,22 +368,22 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
           const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint32_t v[4], o[4];
+            uint32_t v[4];
             int4_word_pairs(wd[c], v);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const __half2 h = *reinterpret_cast<const __half2*>(&v[k]);
               // exact codes: 1024 + q -> q; 1024 + 16 q (odd pairs) -> q
               const __half2 q = (k & 1) ? __hfma2(h, k16, k64) : __hsub2(h, k1024);
-              o[k] = *reinterpret_cast<const uint32_t*>(&q);
+              arow[4 * c + k] = *reinterpret_cast<const uint32_t*>(&q);
             }
-            *reinterpret_cast<uint4*>(A + sw128_off(r, c)) = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
-        fence_proxy_async_smem();   // the MMAs read A through the async proxy
+        tmem_st32(trow + t * slot_cols + a_col, arow);
+        tc_fence_before();   // the MMAs read A after the a_ready handoff
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bar->a_ready[ab]);
+          mbar_arrive(&bar->a_ready[t]);
           mbar_arrive(&bar->empty[s]);
         }
         if (r == 0) GSTAMP(2, gk);
@@ -341,7 +394,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     const int q4 = warp & 3;               // TMEM lane quarter this warp may access
     const int r = q4 * 32 + lane;          // band row
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-    float* xu = reinterpret_cast<float*>(smem + S_XCH);     // [64][65] up values
+    float* ep = reinterpret_cast<float*>(smem + S_EP);      // [128 rows][65] the job's accumulator
     const GemmLayout& G = g.G;
     const ChunkScratch& S = g.S;
     uint32_t fph = 0;
@@ -355,85 +408,91 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     };
     uint32_t gk = 0;
     bool run = true;
-    for (int j = blockIdx.x; run; j += gridDim.x) {
-      Job jb;
-      if (!decode_job(g, j, jb)) break;
+    JobIter it;
+    job_begin(g, it);
+    Job jb;
+    SlotRing sl;
+    while (run && job_next(g, it, jb)) {
       float acc[CHUNK_NT];
 #pragma unroll
       for (int i = 0; i < CHUNK_NT; ++i) acc[i] = 0.f;
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk) {
-        const int ab = gk % DEPTH;
-        // the dequantisation released the side buffer with a_ready (already complete once d_full is)
-        if (!wait(&bar->d_full[ab], (gk / DEPTH) & 1u) || !wait(&bar->a_ready[ab], (gk / DEPTH) & 1u)) {
+      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt)) {
+        const int s = gk % NSG, t = sl.t;
+        // empty[s] completes once the MMAs have finished and the dequantisation (which wrote the side buffer
+        // before arriving) is done
+        if (!wait(&bar->empty[s], (gk / NSG) & 1u)) {
           run = false;
           break;
         }
         tc_fence_after();
         if (r == 0) GSTAMP(4, gk);
-        const uint32_t* side = reinterpret_cast<const uint32_t*>(smem + S_SIDE + ab * SIDE_BYTES);
+        const uint32_t* side = reinterpret_cast<const uint32_t*>(smem + S_SIDE + t * SIDE_BYTES);
         const float2 sb = h2f(side[r]);
-        const float* xs = reinterpret_cast<const float*>(side + 128);
-        const uint32_t d = trow + ab * 128;
+        const float4* xs4 = reinterpret_cast<const float4*>(side + 128);
+        const uint32_t d = trow + t * slot_cols;
 #pragma unroll
         for (int c0 = 0; c0 < CHUNK_NT; c0 += 16) {
           if (c0 < jb.n) {
             uint32_t vh[16], vl[16];
             tmem_ld16_nowait(d + c0, vh);
-            if (jb.lomap >= 0) tmem_ld16_nowait(d + 64 + c0, vl);
+            if (jb.lomap >= 0) tmem_ld16_nowait(d + TM_LO + c0, vl);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float dv = __uint_as_float(vh[i]);
               if (jb.lomap >= 0) dv = fmaf(__uint_as_float(vl[i]), 1.0f / 4096.0f, dv);
-              acc[c0 + i] = fmaf(sb.x, dv, fmaf(sb.y, xs[c0 + i], acc[c0 + i]));
+              const float4 x4 = xs4[(c0 + i) >> 2];
+              const float xv = (i & 3) == 0 ? x4.x : (i & 3) == 1 ? x4.y : (i & 3) == 2 ? x4.z : x4.w;
+              acc[c0 + i] = fmaf(sb.x, dv, fmaf(sb.y, xv, acc[c0 + i]));
             }
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar->d_free[ab]);
+        if (lane == 0) mbar_arrive(&bar->d_free[t]);
         if (r == 0) GSTAMP(5, gk);
       }
       if (!run) break;
-      // ---- epilogue: thread = band row r, columns = the tile's tokens
+      // ---- epilogue. The accumulator goes to shared memory (its register indices are compile-time, so this
+      // is the only unrolled step), then short loops over the tile's tokens write the results: the code that
+      // runs once per job stays small.
+#pragma unroll
+      for (int c0 = 0; c0 < CHUNK_NT; c0 += 16)
+        if (c0 < jb.n)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ep[r * 65 + c0 + i] = acc[c0 + i];
+      if (!fold_sync()) break;
+      const int cnt = jb.cnt;
       if (jb.kind == GK_ROUTER) {
+        // thread = band row (router output row), tokens in a loop; consecutive rows on consecutive lanes
         const int er = jb.m * 128 + r;
         if (er <= G.E)
-#pragma unroll
-          for (int i = 0; i < CHUNK_NT; ++i)
-            if (i < jb.cnt) S.logits[(size_t)(jb.row0 + i) * (G.E + 1) + er] = acc[i];
+#pragma unroll 4
+          for (int i = 0; i < cnt; ++i) S.logits[(size_t)(jb.row0 + i) * (G.E + 1) + er] = ep[r * 65 + i];
       } else if (jb.kind == GK_SHDN || jb.kind == GK_EXDN) {
         float* dst = jb.kind == GK_SHDN ? S.ys : S.y;
-#pragma unroll
-        for (int i = 0; i < CHUNK_NT; ++i)
-          if (i < jb.cnt) dst[(size_t)(jb.row0 + i) * G.H + jb.m * 128 + r] = acc[i];
+#pragma unroll 4
+        for (int i = 0; i < cnt; ++i) dst[(size_t)(jb.row0 + i) * G.H + jb.m * 128 + r] = ep[r * 65 + i];
       } else {
         // SwiGLU: rows 0-63 are gate units 64m.., rows 64-127 the matching up units. h = silu(g) * u is split
-        // into fp16 hi + lo/4096 halves, the down projection's B operand.
+        // into fp16 hi + lo/4096 halves, the down projection's B operand. Thread = (unit u, token parity).
         const bool sh = jb.kind == GK_SHGU;
         const int kd = sh ? G.Is : G.I;
         uint16_t* dhi = sh ? S.hs : S.hh;
         uint16_t* dlo = sh ? S.hs_lo : S.hh_lo;
-        if (r >= 64)
-#pragma unroll
-          for (int i = 0; i < CHUNK_NT; ++i) xu[(r - 64) * 65 + i] = acc[i];
-        if (!fold_sync()) break;
-        if (r < 64) {
-          const int pos = p8u(jb.m * 64 + r);
-#pragma unroll
-          for (int i = 0; i < CHUNK_NT; ++i) {
-            if (i < jb.cnt) {
-              const float h = silu_c(acc[i]) * xu[r * 65 + i];
-              const __half hh = __float2half_rn(h);
-              const __half hl = __float2half_rn((h - __half2float(hh)) * 4096.0f);
-              const size_t o = (size_t)(jb.row0 + i) * kd + pos;
-              dhi[o] = __half_as_ushort(hh);
-              dlo[o] = __half_as_ushort(hl);
-            }
-          }
+        const int u = r & 63;
+        const int pos = p8u(jb.m * 64 + u);
+#pragma unroll 2
+        for (int i = r >> 6; i < cnt; i += 2) {
+          const float h = silu_c(ep[u * 65 + i]) * ep[(u + 64) * 65 + i];
+          const __half hh = __float2half_rn(h);
+          const __half hl = __float2half_rn((h - __half2float(hh)) * 4096.0f);
+          const size_t o = (size_t)(jb.row0 + i) * kd + pos;
+          dhi[o] = __half_as_ushort(hh);
+          dlo[o] = __half_as_ushort(hl);
         }
-        if (!fold_sync()) break;   // the exchange buffer is free for the next job
       }
+      if (!fold_sync()) break;   // the staging buffer is free for the next job
     }
   }
   tc_fence_before();
