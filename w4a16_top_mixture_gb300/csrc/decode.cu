@@ -1137,9 +1137,10 @@ bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch
   pl.grid = grid;
   pl.hp = T == 1 ? L.K : 0;   // h vectors staged in shared memory (one token only)
   const Smem m = smem_map(L, T, grid, pl.hp);
-  // one token: 4 gate/up units a stage keeps every item of the call in the ring at once; more tokens: the ring
-  // wraps anyway, and 8 units (4 unit pairs, 4 warps) a stage put more warps to work on each landed item
-  int SS = (int)((T == 1 ? 4 : 8) * L.EU);
+  // 8 gate/up units (4 unit pairs, 4 warps) a stage. Each bulk copy costs a few hundred nanoseconds of the
+  // SM's copy issue whatever its size, so fewer, larger copies land the routed weights sooner. With one token
+  // the ring then wraps, but only in the routed down rows, whose stages free up long before they are needed.
+  int SS = (int)(8 * L.EU);
   if (SS < 4 * L.H) SS = 4 * L.H;
   if ((int)(2 * L.SU) > SS) SS = (int)(2 * L.SU);
   if ((int)L.RR > SS) SS = (int)L.RR;
