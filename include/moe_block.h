@@ -134,8 +134,10 @@ MOE_API int moe_block_debug_set_wait(moe_block_t *blk, uint32_t timeout_us, int 
  * SM clock stamps (clock64) at its phase boundaries into trace_device[cta * 32 + slot], %globaltimer
  * nanoseconds at the CTA's start and end into slots 30 and 31 (to place every CTA on one time axis), and
  * per-warp clock stamps into trace_device[32 * G + (cta * 16 + warp) * 4 + k] (G = number of SMs). A slot a
- * call does not reach holds 0. trace_device is uint64 device memory of at least 96 * number-of-SMs entries,
- * caller-owned; NULL switches tracing off. */
+ * call does not reach holds 0. A chunk call (T > 16) writes instead the stamps of CTA 0's first 64 K-tiles
+ * of its expert gate/up GEMM launch into trace_device[event * 64 + k], events 0..6: copies issued,
+ * dequantisation start and end, MMAs issued, fold start and end, A seen ready by the MMA issuer. trace_device
+ * is uint64 device memory of at least 96 * number-of-SMs entries, caller-owned; NULL switches tracing off. */
 MOE_API int moe_block_debug_set_trace(moe_block_t *blk, void *trace_device);
 
 /* ---- allocation-free routing ----

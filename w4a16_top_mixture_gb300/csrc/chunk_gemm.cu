@@ -162,7 +162,7 @@ struct Bars {
 };
 
 // debug stamps (CTA 0, first 64 K-tiles): events 0 producer issued, 1 dequant saw the stage, 2 dequant done,
-// 3 MMA issued, 4 fold saw the accumulator, 5 fold done
+// 3 MMA issued, 4 fold saw the accumulator, 5 fold done, 6 MMA saw A ready
 #define GSTAMP(ev, k) do { if (g.trace && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
 
 __device__ __forceinline__ float silu_c(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
