@@ -277,34 +277,71 @@ __global__ void k_chunk_route(const float* __restrict__ logits, int E, int K, in
   }
 }
 
-// One CTA: per-expert token counts from the masks, exclusive scan, the sorted row of every (token, slot), the
-// token of every sorted row, and the list of row tiles (expert, first row, rows <= CHUNK_NT); ctl[0] = count.
-__global__ void k_chunk_bucket(const uint32_t* __restrict__ masks, int E, int TW, int T, int K,
-                               const int32_t* __restrict__ ids, int32_t* __restrict__ slot_of,
-                               int32_t* __restrict__ tok_of, int4* __restrict__ groups, int32_t* __restrict__ ctl) {
-  __shared__ int cnt[512], off[512], ngrp[512], goff[512];
-  const int tid = threadIdx.x;
-  for (int e = tid; e < E; e += blockDim.x) {
-    int c = 0;
-    for (int q = 0; q < TW; ++q) c += __popc(masks[(size_t)e * TW + q]);
-    cnt[e] = c;
-    ngrp[e] = (c + CHUNK_NT - 1) / CHUNK_NT;
+// One CTA of BUCKET_THREADS: per-expert token counts from the masks, exclusive scan, the sorted row of every
+// (token, slot), the token of every sorted row, and the list of row tiles (expert, first row, rows <= CHUNK_NT);
+// ctl[0] = tile count. Tokens of an expert keep their order. With a prefix table (dynamic shared memory of
+// E * TW ints: the tokens of expert e in mask words before word q), a pair's rank is one table read and one
+// mask word; without it (very long chunks) the rank counts the earlier words.
+constexpr int BUCKET_THREADS = 1024;
+constexpr size_t BUCKET_TABLE_MAX = 40960;   // prefix-table bytes that fit beside the static arrays in 48 KB
+__global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t* __restrict__ masks, int E, int TW,
+                                                                 int T, int K, const int32_t* __restrict__ ids,
+                                                                 int32_t* __restrict__ slot_of,
+                                                                 int32_t* __restrict__ tok_of,
+                                                                 int4* __restrict__ groups,
+                                                                 int32_t* __restrict__ ctl, int use_table) {
+  extern __shared__ int pre[];   // [E][TW] when use_table
+  __shared__ int cnt[512], off[512], goff[512], wsum[32], wgsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
+  // counts (thread = expert) and the prefix table
+  int c = 0;
+  if (tid < E) {
+    const uint32_t* m = masks + (size_t)tid * TW;
+#pragma unroll 8
+    for (int q = 0; q < TW; ++q) {
+      if (use_table) pre[tid * TW + q] = c;
+      c += __popc(m[q]);
+    }
+  }
+  const int ng = (c + CHUNK_NT - 1) / CHUNK_NT;
+  // block-wide exclusive scans of the counts and of the tile counts
+  int v = c, gv = ng;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, v, d), gy = __shfl_up_sync(0xFFFFFFFFu, gv, d);
+    if (lane >= d) { v += y; gv += gy; }
+  }
+  if (lane == 31) { wsum[warp] = v; wgsum[warp] = gv; }
+  __syncthreads();
+  if (warp == 0) {
+    int sv = lane < NW ? wsum[lane] : 0, sg = lane < NW ? wgsum[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, sv, d), gy = __shfl_up_sync(0xFFFFFFFFu, sg, d);
+      if (lane >= d) { sv += y; sg += gy; }
+    }
+    if (lane < NW) { wsum[lane] = sv; wgsum[lane] = sg; }   // inclusive over warps
   }
   __syncthreads();
-  if (tid == 0) {
-    int o = 0, go = 0;
-    for (int e = 0; e < E; ++e) { off[e] = o; o += cnt[e]; goff[e] = go; go += ngrp[e]; }
-    ctl[0] = go;
+  if (tid < E) {
+    cnt[tid] = c;
+    off[tid] = (warp > 0 ? wsum[warp - 1] : 0) + v - c;
+    goff[tid] = (warp > 0 ? wgsum[warp - 1] : 0) + gv - ng;
   }
+  if (tid == 0) ctl[0] = wgsum[NW - 1];
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x)
-    for (int g = 0; g < ngrp[e]; ++g)
+    for (int g = 0; g * CHUNK_NT < cnt[e]; ++g)
       groups[goff[e] + g] = make_int4(e, off[e] + g * CHUNK_NT, min(CHUNK_NT, cnt[e] - g * CHUNK_NT), 0);
   for (int p = tid; p < T * K; p += blockDim.x) {
     const int t = p / K, e = ids[p];
-    int rank = 0;
     const uint32_t* m = masks + (size_t)e * TW;
-    for (int q = 0; q < (t >> 5); ++q) rank += __popc(m[q]);
+    int rank = 0;
+    if (use_table) {
+      rank = pre[e * TW + (t >> 5)];
+    } else {
+      for (int q = 0; q < (t >> 5); ++q) rank += __popc(m[q]);
+    }
     rank += __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
     const int row = off[e] + rank;
     slot_of[p] = row;
@@ -357,7 +394,11 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   k_chunk_route<<<(T + 7) / 8, 256, 0, st>>>(S.logits, E, K, T, S.ids, S.w, S.sg, S.masks, TW, rec_ids, rec_w,
                                               rec_sg);
   ++n;
-  k_chunk_bucket<<<1, 512, 0, st>>>(S.masks, E, TW, T, K, S.ids, S.slot_of, S.tok_of, S.groups, S.ctl);
+  // the prefix table fits in shared memory for chunks up to tens of thousands of tokens
+  const size_t tbl = (size_t)E * TW * sizeof(int);
+  const int use_table = tbl <= BUCKET_TABLE_MAX ? 1 : 0;
+  k_chunk_bucket<<<1, BUCKET_THREADS, use_table ? tbl : 0, st>>>(S.masks, E, TW, T, K, S.ids, S.slot_of, S.tok_of,
+                                                                 S.groups, S.ctl, use_table);
   ++n;
   k_chunk_gather<<<(T * K + 7) / 8, 256, 0, st>>>(S.xp, S.tok_of, T * K, H, S.xs);
   ++n;
