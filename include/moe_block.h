@@ -158,6 +158,13 @@ MOE_API int moe_router_topk_noalloc(const uint8_t *router_q, const uint16_t *rou
 /* Number of CUDA kernel launches the last forward call made. */
 MOE_API int moe_block_last_launch_count(moe_block_t *blk);
 
+/* Host-only planning query (no device, no allocation): the launch plan the fused decode kernel uses for a call
+ * of T tokens on a device with num_sms SMs and max_smem bytes of opt-in shared memory per block. On MOE_OK,
+ * out[0..4] = grid (CTAs), dynamic shared memory bytes, ring stages, bytes per stage, and h vectors staged in
+ * shared memory. MOE_ERR_UNSUPPORTED: the shape or T has no decode plan (T > 16 uses the chunk path);
+ * MOE_ERR_INVALID_ARG: a NULL pointer or a non-positive size. */
+MOE_API int moe_debug_decode_plan(const moe_block_config_t *cfg, int T, int num_sms, int max_smem, int32_t *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -88,9 +88,8 @@ static void free_all(moe_block* b) {
   cudaFree(b->cscratch);
 }
 
-extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out) {
-  if (!cfg || !out) return MOE_ERR_INVALID_ARG;
-  const moe_block_config_t c = *cfg;
+// the shapes the library has kernels for (MOE_OK) or not (MOE_ERR_UNSUPPORTED)
+static int check_config(const moe_block_config_t& c) {
   if (c.group_size != 64) return MOE_ERR_UNSUPPORTED;
   if (c.hidden != 512 && c.hidden != 1024 && c.hidden != 2048) return MOE_ERR_UNSUPPORTED;
   if (c.n_experts < 1 || c.n_experts > 512) return MOE_ERR_UNSUPPORTED;
@@ -98,6 +97,34 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   if (c.expert_inter < 64 || c.expert_inter > 1024 || c.expert_inter % 64) return MOE_ERR_UNSUPPORTED;
   if (c.shared_inter < 64 || c.shared_inter > 1024 || c.shared_inter % 64) return MOE_ERR_UNSUPPORTED;
   if (c.max_tokens < 1 || c.max_tokens > 4096) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+extern "C" int moe_debug_decode_plan(const moe_block_config_t* cfg, int T, int num_sms, int max_smem,
+                                     int32_t* out) {
+  if (!cfg || !out || T < 1 || num_sms < 1 || max_smem < 1) return MOE_ERR_INVALID_ARG;
+  const int st = check_config(*cfg);
+  if (st != MOE_OK) return st;
+  const MoeLayout L = moe_make_layout(cfg->hidden, cfg->n_experts, cfg->top_k, cfg->expert_inter,
+                                      cfg->shared_inter);
+  if (!decode_supported(L)) return MOE_ERR_UNSUPPORTED;
+  DecodeLaunch pl;
+  if (!decode_plan(L, T, num_sms, max_smem, &pl)) return MOE_ERR_UNSUPPORTED;
+  out[0] = pl.grid;
+  out[1] = pl.smem;
+  out[2] = pl.NS;
+  out[3] = pl.SS;
+  out[4] = pl.hp;
+  return MOE_OK;
+}
+
+extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out) {
+  if (!cfg || !out) return MOE_ERR_INVALID_ARG;
+  const moe_block_config_t c = *cfg;
+  {
+    const int st = check_config(c);
+    if (st != MOE_OK) return st;
+  }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_NO_DEVICE;
   cudaDeviceProp prop;

@@ -23,7 +23,7 @@ EXPORTS = ["moe_block_create", "moe_block_load_weights", "moe_block_forward", "m
            "moe_block_forward_residual", "moe_block_get_status", "moe_block_destroy", "moe_block_strerror",
            "moe_last_cuda_error", "moe_block_debug_dequant", "moe_block_debug_last_routing",
            "moe_block_debug_set_wait", "moe_block_debug_set_trace", "moe_block_last_launch_count",
-           "moe_router_topk_noalloc"]
+           "moe_router_topk_noalloc", "moe_debug_decode_plan"]
 
 
 class MoeError(RuntimeError):
@@ -77,11 +77,24 @@ def load_library(path: str = LIB_PATH):
     lib.moe_block_last_launch_count.argtypes = [vp]
     lib.moe_block_debug_set_trace.argtypes = [vp, vp]
     lib.moe_router_topk_noalloc.argtypes = [vp, vp, vp, i, i, i, vp, i, vp, vp, vp, vp]
+    lib.moe_debug_decode_plan.argtypes = [ctypes.POINTER(Config), i, i, i, ctypes.POINTER(ctypes.c_int32)]
     for n in EXPORTS:
         if not hasattr(lib, n):
             raise RuntimeError(f"{path} does not export {n}")
     _LIB = lib
     return lib
+
+
+def decode_plan(cfg, T, num_sms, max_smem):
+    """Host-only query of the fused decode kernel's launch plan (no device needed): (status, plan), plan a dict
+    of grid, smem, stages, stage_bytes, h_staged when status == 0."""
+    lib = load_library()
+    c = Config(cfg.hidden, cfg.n_experts, cfg.top_k, cfg.expert_inter, cfg.shared_inter, 64, 16)
+    out = (ctypes.c_int32 * 5)()
+    st = lib.moe_debug_decode_plan(ctypes.byref(c), int(T), int(num_sms), int(max_smem), out)
+    if st != MOE_OK:
+        return st, None
+    return st, dict(zip(("grid", "smem", "stages", "stage_bytes", "h_staged"), list(out)))
 
 
 def _check(status, what):
