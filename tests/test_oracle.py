@@ -288,7 +288,49 @@ def _swiglu_sigmoid_not_silu(Wg, Wu, Wd, x):
     return h @ Wd.T, h
 
 
+_orig_block = O.block_forward
+_orig_rmsnorm = O.rmsnorm
+
+
+def _block_shared_gate_ignored(w, x, top_k, *args, **kw):
+    r = _orig_block(w, x, top_k, *args, **kw)
+    r["out"] = r["routed"] + r["shared"]
+    return r
+
+
+def _block_shared_dropped(w, x, top_k, *args, **kw):
+    r = _orig_block(w, x, top_k, *args, **kw)
+    r["out"] = r["routed"].copy()
+    return r
+
+
+def _rmsnorm_no_gamma(h, gamma, eps=1e-6):
+    return _orig_rmsnorm(h, np.ones_like(np.asarray(gamma, np.float64)), eps)
+
+
+def _rmsnorm_eps_outside(h, gamma, eps=1e-6):
+    h = np.asarray(h, np.float64)
+    return h / (np.sqrt(np.mean(h * h, axis=-1, keepdims=True)) + eps) * np.asarray(gamma, np.float64)
+
+
+def _stack_residual_dropped(layers, h0, top_k, eps=1e-6, group=64):
+    h = np.asarray(h0, np.float64)
+    recs = []
+    for w in layers:
+        xn = O.rmsnorm(h, w["rms_gamma"], eps)
+        r = O.block_forward(w, xn, top_k, group)
+        r["h_in"], r["x_norm"] = h, xn
+        h = r["out"]
+        recs.append(r)
+    return h, recs
+
+
 MUTANTS = {
+    "shared_gate_ignored": dict(block_forward=_block_shared_gate_ignored),
+    "shared_expert_dropped": dict(block_forward=_block_shared_dropped),
+    "rmsnorm_no_gamma": dict(rmsnorm=_rmsnorm_no_gamma),
+    "rmsnorm_eps_outside_sqrt": dict(rmsnorm=_rmsnorm_eps_outside),
+    "residual_dropped": dict(stack_forward=_stack_residual_dropped),
     "nibble_order": dict(unpack_int4=_swapped_nibbles),
     "scale_bias_swap": dict(dequant=_dequant_swapped_sb),
     "group_index": dict(dequant=_dequant_group32),
