@@ -84,7 +84,7 @@ def traffic_record():
 def kernel_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a16_top_mixture_gb300", "csrc")
-    for f in ("decode.cu", "decode.cuh", "layout.cuh", "ptx.cuh"):   # the sources k_decode is built from
+    for f in ("decode1.cu", "decode_dev.cuh", "decode.cuh", "layout.cuh", "ptx.cuh"):   # k_decode1's sources
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
@@ -407,7 +407,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": tr, "peak_kind": kind,
                          "algorithmic_bytes_per_launch": bytes_call,
-                         "kernel": "k_decode (fused decode kernel, one launch per step)"},
+                         "kernel": "k_decode1 (fused single-token decode kernel, one launch per step)"},
             "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{cpu_d['tokens']} T=1 tokens through one production block in "
                                        f"{cpu_d['seconds']:.1f} s, single-threaded float64 numpy"},

@@ -71,3 +71,18 @@ def check_tol(out_gpu, out_ref, tol=2e-3):
     rms = np.sqrt(np.mean(ref * ref))
     excess = (err - half_ulp16(ref)).clip(min=0.0).max() / rms
     return bool(excess <= tol), float(excess), float(err.max() / rms)
+
+
+def quantize_acts(x, chunk=32):
+    """The decode kernels' activation grid, written out: every 32-column chunk of a token is scaled by the power
+    of two 2^(15 - e) (e the least integer with max|x_chunk| < 2^e), rounded to the nearest integer (ties to
+    even) and clamped to +-32767, then scaled back. The kernels' integer dot products are exact on these
+    values, so the oracle evaluated at quantize_acts(x) predicts the kernels' logits up to fp32 rounding."""
+    x = np.asarray(x, np.float64)
+    T, H = x.shape
+    xc = x.reshape(T, H // chunk, chunk)
+    m = np.abs(xc).max(-1, keepdims=True)
+    e = np.where(m > 0, np.floor(np.log2(np.where(m > 0, m, 1.0))) + 1, -111)
+    sc = 2.0 ** (15 - e)
+    q = np.clip(np.rint(xc * sc), -32767, 32767)
+    return (q / sc).reshape(T, H)

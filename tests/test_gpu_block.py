@@ -1,11 +1,12 @@
 """CUDA path vs the float64 oracle, through the C ABI (ctypes). Dequantised weights and expert ids must match
 bit for bit; outputs within 2e-3 * RMS(out_oracle) beyond the fp16 output's own rounding (fp16 output, fp32
-accumulation; see tests._cases.check_tol)."""
+accumulation; see tests._cases.check_tol); router logits, routing weights and the sigmoid gate within the bounds
+checked against the oracle at the decode kernels' activation grid (tests._cases.quantize_acts)."""
 import numpy as np
 import pytest
 
 import oracle.moe_oracle as O
-from tests._cases import check_tol, make_case, rel_err, structural
+from tests._cases import check_tol, make_case, quantize_acts, rel_err, structural
 from w4a16_top_mixture_gb300 import build, lib, synth
 
 pytestmark = pytest.mark.gpu
@@ -39,14 +40,19 @@ def run(blk, x):
     return out.cpu().numpy().astype(np.float64), xd, out
 
 
-def check_routing(blk, r, T, K):
+def check_routing(blk, r, T, K, w, x):
+    """Ids bit-exact against the oracle on the block's input. Logits, routing weights and the sigmoid gate against
+    the oracle evaluated at the kernels' own activation grid (tests._cases.quantize_acts), where only fp32
+    rounding separates them."""
     rt = blk.last_routing(T)
     ids = rt["ids"].cpu().numpy()
     np.testing.assert_array_equal(ids, r["ids"])
-    np.testing.assert_allclose(rt["w"].cpu().numpy(), r["w"], rtol=0, atol=2e-5)
-    np.testing.assert_allclose(rt["sg"].cpu().numpy(), r["sg"], rtol=0, atol=2e-6)
-    np.testing.assert_allclose(rt["logits"].cpu().numpy(), r["logits"], rtol=0,
-                               atol=2e-5 * np.abs(r["logits"]).max())
+    rq = O.block_forward(w, quantize_acts(x), K)
+    np.testing.assert_array_equal(ids, rq["ids"])
+    np.testing.assert_allclose(rt["w"].cpu().numpy(), rq["w"], rtol=0, atol=2e-5)
+    np.testing.assert_allclose(rt["sg"].cpu().numpy(), rq["sg"], rtol=0, atol=2e-6)
+    np.testing.assert_allclose(rt["logits"].cpu().numpy(), rq["logits"], rtol=0,
+                               atol=2e-5 * np.abs(rq["logits"]).max())
 
 
 # ---------------------------------------------------------------- dequantisation, bit-exact
@@ -83,7 +89,7 @@ def test_tiny_t1(seed):
     r = O.block_forward(w, x, cfg.top_k)
     blk = make_block(cfg, w)
     out, _, _ = run(blk, x)
-    check_routing(blk, r, 1, cfg.top_k)
+    check_routing(blk, r, 1, cfg.top_k, w, x)
     ok, e, plain = check_tol(out, r["out"])
     assert ok, (e, plain)
     cos, ratio, moved = structural(out, r)
@@ -123,7 +129,7 @@ def test_prod_t1(prod_block, seed):
     x = _prod_tokens(cfg, w, 1, 1000 + seed)
     r = O.block_forward(w, x, cfg.top_k)
     out, _, _ = run(blk, x)
-    check_routing(blk, r, 1, cfg.top_k)
+    check_routing(blk, r, 1, cfg.top_k, w, x)
     ok, e, plain = check_tol(out, r["out"])
     print(f"prod T=1 seed {seed}: err beyond fp16 rounding/RMS = {e:.3e} (plain {plain:.3e})")
     assert ok, (e, plain)
@@ -137,7 +143,7 @@ def test_prod_ragged_batches(prod_block, T):
     x = _prod_tokens(cfg, w, T, 2000 + T)
     r = O.block_forward(w, x, cfg.top_k)
     out, _, _ = run(blk, x)
-    check_routing(blk, r, T, cfg.top_k)
+    check_routing(blk, r, T, cfg.top_k, w, x)
     ok, e, plain = check_tol(out, r["out"])
     print(f"prod T={T}: err beyond fp16 rounding/RMS = {e:.3e} (plain {plain:.3e})")
     assert ok, (e, plain)
@@ -150,7 +156,7 @@ def test_prod_t16_zipf():
     U = len(np.unique(r["ids"]))
     blk = make_block(cfg, w)
     out, _, _ = run(blk, x)
-    check_routing(blk, r, 16, cfg.top_k)
+    check_routing(blk, r, 16, cfg.top_k, w, x)
     ok, e, plain = check_tol(out, r["out"])
     print(f"zipf T=16: {U} unique experts, err beyond fp16 rounding/RMS = {e:.3e} (plain {plain:.3e})")
     assert U < 16 * cfg.top_k      # reuse across tokens

@@ -26,8 +26,8 @@ def test_every_decode_token_count_has_a_plan(cfg):
         assert pl["stage_bytes"] % 128 == 0
         assert 4 <= pl["stages"] <= 24
         assert pl["stages"] * pl["stage_bytes"] <= pl["smem"] <= SMEM
-        # h vectors of the selected experts are staged in shared memory for a single token only
-        assert pl["h_staged"] == (cfg.top_k if T == 1 else 0)
+        # the multi-token kernel reads each pair's h from L2 (the single-token kernel stages them itself)
+        assert pl["h_staged"] == 0
         stage_bytes.add(pl["stage_bytes"])
     # one stage size (8 gate/up units) for every token count
     assert len(stage_bytes) == 1

@@ -28,11 +28,15 @@ struct moe_block {
   int32_t* rec_ids = nullptr;
   float *rec_w = nullptr, *rec_sg = nullptr;
   uint16_t *xbuf = nullptr, *obuf = nullptr;       // staging for forward_host
+  uint32_t* status_host = nullptr;                 // pinned copy of the status word (forward_host)
   uint64_t timeout_ns = 500ull * 1000 * 1000;
   int skip_arrive = 0;
   int last_launches = 0;
   int last_T = 0;
   DecodeLaunch plans[DEC_TMAX + 1];                // launch plan per T, computed at create
+  bool has_dec1 = false;                           // the single-token kernel serves T = 1
+  Decode1Launch plan1;
+  cudaStream_t last_stream = nullptr;              // stream of the last forward call (for get_status)
   uint64_t* trace = nullptr;                       // optional phase-timestamp buffer (debug)
   // prompt-chunk path (T > 16): GEMM-layout weight copy and its scratch, only when max_tokens > 16
   bool chunk = false;
@@ -86,6 +90,7 @@ static void free_all(moe_block* b) {
   cudaFree(b->obuf);
   cudaFree(b->gstore);
   cudaFree(b->cscratch);
+  cudaFreeHost(b->status_host);
 }
 
 // the shapes the library has kernels for (MOE_OK) or not (MOE_ERR_UNSUPPORTED)
@@ -149,6 +154,7 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   for (int T = 1; T <= b->dec_T; ++T) {
     if (!decode_plan(b->L, T, b->num_sms, b->max_smem, &b->plans[T])) { delete b; return MOE_ERR_UNSUPPORTED; }
   }
+  b->has_dec1 = decode1_plan(b->L, b->num_sms, b->max_smem, &b->plan1);
   const MoeLayout& L = b->L;
   size_t total = L.router_bytes + L.shgu_bytes + L.shdn_bytes + L.exgu_bytes + L.exdn_bytes;
   cudaError_t e = cudaMalloc(&b->wstore, total);
@@ -171,6 +177,8 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   if (e == cudaSuccess) e = cudaMalloc(&b->rec_sg, (size_t)c.max_tokens * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->xbuf, (size_t)c.max_tokens * c.hidden * 2);
   if (e == cudaSuccess) e = cudaMalloc(&b->obuf, (size_t)c.max_tokens * c.hidden * 2);
+  if (e == cudaSuccess) e = cudaHostAlloc(&b->status_host, 16, cudaHostAllocDefault);
+  if (e == cudaSuccess) *b->status_host = 0;
   if (e == cudaSuccess && c.max_tokens > DEC_TMAX) {
     b->chunk = true;
     e = cudaMalloc(&b->gstore, gemm_store_bytes(L));
@@ -257,10 +265,39 @@ extern "C" int moe_block_load_weights(moe_block_t* b, const moe_block_weights_t*
   return MOE_OK;
 }
 
+static DecodeArgs decode_args(moe_block* b, const uint16_t* x, uint16_t* out, uint16_t* out2, int T, int t0,
+                              const uint16_t* gamma, float eps) {
+  DecodeArgs a;
+  a.router = b->router; a.sh_gu = b->sh_gu; a.sh_dn = b->sh_dn; a.ex_gu = b->ex_gu; a.ex_dn = b->ex_dn;
+  a.x = x + (size_t)t0 * b->cfg.hidden;
+  a.out = out + (size_t)t0 * b->cfg.hidden;
+  a.out2 = out2 ? out2 + (size_t)t0 * b->cfg.hidden : nullptr;
+  a.gamma = gamma;
+  a.eps = eps;
+  a.T = T;
+  a.logits = b->logits; a.hs = b->hs; a.hbuf = b->hbuf;
+  a.counters = b->counters; a.status = b->status;
+  a.rec_ids = b->rec_ids + (size_t)t0 * b->cfg.top_k;
+  a.rec_w = b->rec_w + (size_t)t0 * b->cfg.top_k;
+  a.rec_sg = b->rec_sg + t0;
+  a.timeout_ns = b->timeout_ns;
+  a.skip_arrive = b->skip_arrive;
+  a.trace = b->trace;
+  b->skip_arrive = 0;
+  return a;
+}
+
 static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, const uint16_t* gamma, float eps,
-                       cudaStream_t st) {
+                       cudaStream_t st, uint16_t* out2 = nullptr) {
   b->last_launches = 0;
   b->last_T = T;
+  b->last_stream = st;
+  if (T == 1 && b->has_dec1) {
+    cudaError_t e = decode1_launch(b->L, decode_args(b, x, out, out2, 1, 0, gamma, eps), b->plan1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    b->last_launches = 1;
+    return MOE_OK;
+  }
   if (T > DEC_TMAX && b->chunk) {
     int n = 0;
     cudaError_t e = chunk_forward(b->L, b->G, b->CS, b->maps, b->cfg.max_tokens, b->num_sms, x, out, T, gamma, eps,
@@ -273,22 +310,7 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
   for (int t0 = 0; t0 < T; t0 += DEC_TMAX) {
     const int n = T - t0 < DEC_TMAX ? T - t0 : DEC_TMAX;
     const DecodeLaunch& pl = b->plans[n];
-    DecodeArgs a;
-    a.router = b->router; a.sh_gu = b->sh_gu; a.sh_dn = b->sh_dn; a.ex_gu = b->ex_gu; a.ex_dn = b->ex_dn;
-    a.x = x + (size_t)t0 * b->cfg.hidden;
-    a.out = out + (size_t)t0 * b->cfg.hidden;
-    a.gamma = gamma;
-    a.eps = eps;
-    a.T = n;
-    a.logits = b->logits; a.hs = b->hs; a.hbuf = b->hbuf;
-    a.counters = b->counters; a.status = b->status;
-    a.rec_ids = b->rec_ids + (size_t)t0 * b->cfg.top_k;
-    a.rec_w = b->rec_w + (size_t)t0 * b->cfg.top_k;
-    a.rec_sg = b->rec_sg + t0;
-    a.timeout_ns = b->timeout_ns;
-    a.skip_arrive = b->skip_arrive;
-    a.trace = b->trace;
-    b->skip_arrive = 0;
+    const DecodeArgs a = decode_args(b, x, out, out2, n, t0, gamma, eps);
     cudaError_t e = decode_launch(b->L, a, pl, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     ++b->last_launches;
@@ -329,19 +351,25 @@ extern "C" int moe_block_forward_host(moe_block_t* b, const void* x_host, void* 
   int s = run_forward(b, b->xbuf, b->obuf, T, nullptr, 0.f, st);
   if (s != MOE_OK) return s;
   CK(cudaMemcpyAsync(out_host, b->obuf, bytes, cudaMemcpyDeviceToHost, st));
+  CK(cudaMemcpyAsync(b->status_host, b->status, 4, cudaMemcpyDeviceToHost, st));
   CK(cudaStreamSynchronize(st));
+  // the call has completed: a bounded device wait that ran out is reported here (the handle's device state is
+  // reset as in moe_block_get_status)
+  if (*b->status_host) return moe_block_get_status(b, nullptr);
   return MOE_OK;
 }
 
 extern "C" int moe_block_get_status(moe_block_t* b, uint32_t* flags) {
   if (!b) return MOE_ERR_INVALID_ARG;
-  CK(cudaDeviceSynchronize());
+  // the handle's device work: everything issued to the stream of its last forward call
+  CK(cudaStreamSynchronize(b->last_stream));
   uint32_t st = 0;
   CK(cudaMemcpy(&st, b->status, 4, cudaMemcpyDeviceToHost));
   if (flags) *flags = st;
   if (st) {
     CK(cudaMemset(b->counters, 0, 8 * 4));
     CK(cudaDeviceSynchronize());
+    if (b->status_host) *b->status_host = 0;
     return MOE_ERR_DEVICE_TIMEOUT;
   }
   return MOE_OK;
@@ -358,6 +386,27 @@ extern "C" int moe_block_debug_dequant(moe_block_t* b, int which, int index, flo
   return MOE_OK;
 }
 
+// Each token's k (id, weight) pairs of the routing record into ascending id order (the single-token kernel records
+// them in selection order); one thread per token, insertion sort. Idempotent.
+__global__ void k_sort_routing(int32_t* ids, float* w, int T, int K) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  int32_t* id = ids + (size_t)t * K;
+  float* wt = w + (size_t)t * K;
+  for (int i = 1; i < K; ++i) {
+    const int32_t ki = id[i];
+    const float wi = wt[i];
+    int j = i - 1;
+    while (j >= 0 && id[j] > ki) {
+      id[j + 1] = id[j];
+      wt[j + 1] = wt[j];
+      --j;
+    }
+    id[j + 1] = ki;
+    wt[j + 1] = wi;
+  }
+}
+
 extern "C" int moe_block_debug_last_routing(moe_block_t* b, int T, float* logits, int32_t* ids, float* w,
                                             float* sg, void* stream) {
   if (!b || T < 1 || T > b->last_T) return MOE_ERR_INVALID_ARG;
@@ -365,6 +414,8 @@ extern "C" int moe_block_debug_last_routing(moe_block_t* b, int T, float* logits
   cudaStream_t st = (cudaStream_t)stream;
   const int E = b->cfg.n_experts, K = b->cfg.top_k;
   if (logits) CK(cudaMemcpyAsync(logits, b->logits, (size_t)T * (E + 1) * 4, cudaMemcpyDeviceToDevice, st));
+  k_sort_routing<<<(T + 127) / 128, 128, 0, st>>>(b->rec_ids, b->rec_w, T, K);
+  CK(cudaGetLastError());
   if (ids) CK(cudaMemcpyAsync(ids, b->rec_ids, (size_t)T * K * 4, cudaMemcpyDeviceToDevice, st));
   if (w) CK(cudaMemcpyAsync(w, b->rec_w, (size_t)T * K * 4, cudaMemcpyDeviceToDevice, st));
   if (sg) CK(cudaMemcpyAsync(sg, b->rec_sg, (size_t)T * 4, cudaMemcpyDeviceToDevice, st));

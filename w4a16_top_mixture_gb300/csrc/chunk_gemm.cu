@@ -30,6 +30,7 @@
 //              that read A are complete too                          (fold -> dequantisation)
 // Keeping A out of shared memory leaves the shared-memory pipe to the copies, the code loads and B.
 // Every wait is bounded; on a timeout the CTA records an error bit and every role leaves its loops.
+#include <mutex>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -503,12 +504,22 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
 
 }  // namespace
 
+static std::mutex g_gemm_attr_mutex;
+
 cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_chunk_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
+  // the shared-memory limit is a per-device setting of the function: raise it once on every device used
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(g_gemm_attr_mutex);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(k_chunk_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
   }
   k_chunk_gemm<<<grid, GTH, GEMM_SMEM, st>>>(g);
   return cudaGetLastError();

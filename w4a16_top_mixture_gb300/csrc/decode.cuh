@@ -13,6 +13,8 @@ constexpr int DEC_MAXSEG = 4;                     // expert segments one CTA's u
 constexpr int DEC_MAXROWS = 32;                   // output rows one CTA owns (ceil(H / grid))
 constexpr int DEC_MAXNS = 24;                     // ring stages
 constexpr int DEC_MAXGRID = 160;                  // CTAs (one per SM)
+constexpr int DEC1_NCW = 12;                      // consumer warps of the single-token kernel
+constexpr int DEC1_THREADS = (DEC1_NCW + 1) * 32; // + one producer warp
 
 // device error bits
 enum : uint32_t {
@@ -24,6 +26,7 @@ struct DecodeArgs {
   const uint8_t *router, *sh_gu, *sh_dn, *ex_gu, *ex_dn;
   const uint16_t* x;        // [T][H] fp16 (h_in in residual mode)
   uint16_t* out;            // [T][H] fp16
+  uint16_t* out2;           // optional second copy of out (a stacked layer's per-layer record); may be null
   const uint16_t* gamma;    // non-null: residual mode, x_hat = RMSNorm(x), out = x + block(x_hat)
   float eps;
   int T;
@@ -44,10 +47,20 @@ struct DecodeLaunch {
   int grid, smem, NS, SS, hp;   // hp: routed h vectors staged in shared memory (one token: K; else 0)
 };
 
+// Launch plan of the single-token kernel: grid, dynamic shared memory, and whether two CTAs fit on one SM
+// (so that the next call's CTAs can be resident while this call runs).
+struct Decode1Launch {
+  int grid, smem, two_per_sm;
+};
+
 // Host: shared-memory plan for a call with T tokens; returns false if it does not fit.
 bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch* out);
 bool decode_supported(const MoeLayout& L);   // shapes with a compiled decode kernel
 cudaError_t decode_launch(const MoeLayout& L, const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st);
 size_t decode_hbuf_floats(const MoeLayout& L, int T);
+
+// Host: plan of the single-token kernel (T = 1); false if the shape has no such kernel or it does not fit.
+bool decode1_plan(const MoeLayout& L, int grid, int max_smem, Decode1Launch* out);
+cudaError_t decode1_launch(const MoeLayout& L, const DecodeArgs& a, const Decode1Launch& pl, cudaStream_t st);
 
 }  // namespace moe

@@ -1,10 +1,8 @@
-// Inline-PTX helpers for sm_103a: mbarriers, 1-D bulk async copies (TMA engine), globaltimer, and the code
-// unpacking used by every dot product. Unpacking relies only on IEEE-754 encoding facts:
-//   * a float whose exponent field is that of 2^23 and whose low mantissa bits hold an integer v (< 2^23) is
-//     exactly 2^23 + v, so OR-ing a code field into 0x4B000000 in place and removing 2^23 by an exact fused
-//     multiply-add recovers the code as a float with no integer-to-float conversion;
-//   * codes left at bit position 4k (or 8k) come out multiplied by 2^(4k) (2^(8k)); the same fused step
-//     multiplies by the exact power of two 2^-4k (2^-8k).
+// Inline-PTX helpers for sm_103a: mbarriers, 1-D bulk async copies (TMA engine), globaltimer, bounded waits,
+// and the code-to-fp16 unpacking of the prompt-chunk GEMM. That unpacking relies only on an IEEE-754 encoding
+// fact: an fp16 value whose exponent field is that of 1024 and whose low mantissa bits hold an integer v < 1024
+// is exactly 1024 + v, so OR-ing a code field into 0x6400 yields 1024 + code (or 1024 + 16 code for a field at
+// bit 4) with no integer-to-float conversion.
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -61,9 +59,9 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false if the phase did not complete within timeout_ns. The loop is kept out of line
-// so that the many call sites share one copy of it (instruction-cache footprint).
-__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+// Bounded wait: returns false if the phase did not complete within timeout_ns. The loop is kept out of line so
+// that the many call sites share one copy of it (instruction-cache footprint of the kernels).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
@@ -107,9 +105,15 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-// Bounded spin until *cnt >= target. Returns false on timeout.
-__device__ __forceinline__ bool spin_geq(const uint32_t* cnt, uint32_t target, uint64_t timeout_ns) {
-  if (ld_acquire_u32(cnt) >= target) return true;
+// *cnt += v with release semantics at GPU scope: every write this thread made before (and every write it has
+// observed, e.g. through a preceding barrier) is visible to a thread that later reads the new count with an
+// acquire load (ld_acquire_u32). One instruction in place of a full fence followed by an atomic.
+__device__ __forceinline__ void red_release_add(uint32_t* cnt, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(cnt), "r"(v) : "memory");
+}
+
+// Bounded spin until *cnt >= target. Returns false on timeout. The loop is out of line (one copy per kernel).
+static __device__ __noinline__ bool spin_geq_slow(const uint32_t* cnt, uint32_t target, uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 8; ++i) {
@@ -119,72 +123,12 @@ __device__ __forceinline__ bool spin_geq(const uint32_t* cnt, uint32_t target, u
     if (globaltimer() - t0 > timeout_ns) return false;
   }
 }
-
-constexpr uint32_t MAGIC = 0x4B000000u;   // bit pattern of 2^23
-
-__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
-__device__ __forceinline__ float bits(uint32_t v) { return __uint_as_float(v); }
-
-// One 32-bit word of int4 codes (element n of the word in bits 4n..4n+3) -> the pairs
-// (q_k, q_{4+k}) for k = 0..3, exact, as floats.
-__device__ __forceinline__ void unpack_int4_word(uint32_t w, float2 q[4]) {
-  const uint32_t hi = w >> 16;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t m = 0xFu << (4 * k);
-    const float sc = __uint_as_float((uint32_t)(127 - 4 * k) << 23);            // 2^-4k
-    const float off = -__uint_as_float((uint32_t)(127 + 23 - 4 * k) << 23);     // -2^(23-4k)
-    q[k] = __ffma2_rn(f2(bits((w & m) | MAGIC), bits((hi & m) | MAGIC)), f2(sc, sc), f2(off, off));
-  }
-}
-
-// Two 32-bit words of int8 codes (columns 0..3 in w0, 4..7 in w1, column n in byte n%4) -> the pairs
-// (q_k, q_{4+k}) for k = 0..3, exact.
-__device__ __forceinline__ void unpack_int8_pair(uint32_t w0, uint32_t w1, float2 q[4]) {
-  const uint32_t h0 = w0 >> 16, h1 = w1 >> 16;
-  const float s8 = __uint_as_float((uint32_t)(127 - 8) << 23);          // 2^-8
-  const float o0 = -8388608.0f;                                         // -2^23
-  const float o8 = -__uint_as_float((uint32_t)(127 + 15) << 23);        // -2^15
-  q[0] = __ffma2_rn(f2(bits((w0 & 0xFFu) | MAGIC), bits((w1 & 0xFFu) | MAGIC)), f2(1.f, 1.f), f2(o0, o0));
-  q[1] = __ffma2_rn(f2(bits((w0 & 0xFF00u) | MAGIC), bits((w1 & 0xFF00u) | MAGIC)), f2(s8, s8), f2(o8, o8));
-  q[2] = __ffma2_rn(f2(bits((h0 & 0xFFu) | MAGIC), bits((h1 & 0xFFu) | MAGIC)), f2(1.f, 1.f), f2(o0, o0));
-  q[3] = __ffma2_rn(f2(bits((h0 & 0xFF00u) | MAGIC), bits((h1 & 0xFF00u) | MAGIC)), f2(s8, s8), f2(o8, o8));
-}
-
-// One 32-bit word of int8 codes (column n in byte n) -> (q0, q1), (q2, q3), exact.
-__device__ __forceinline__ void unpack_int8_word(uint32_t w, float2& q01, float2& q23) {
-  const uint32_t h = w >> 16;
-  const float s8 = 0.00390625f;
-  q01 = __ffma2_rn(f2(bits((w & 0xFFu) | MAGIC), bits((w & 0xFF00u) | MAGIC)), f2(1.f, s8), f2(-8388608.0f, -32768.0f));
-  q23 = __ffma2_rn(f2(bits((h & 0xFFu) | MAGIC), bits((h & 0xFF00u) | MAGIC)), f2(1.f, s8), f2(-8388608.0f, -32768.0f));
-}
-
-// Four int4 codes of a 16-bit field (columns 4m..4m+3 of a canonically packed int4 row) -> (q0, q1), (q2, q3),
-// exact.
-__device__ __forceinline__ void unpack_int4_quad(uint32_t hw, float2& q01, float2& q23) {
-  const float a = bits((hw & 0xFu) | MAGIC), b = bits((hw & 0xF0u) | MAGIC);
-  const float c = bits((hw & 0xF00u) | MAGIC), d = bits((hw & 0xF000u) | MAGIC);
-  q01 = __ffma2_rn(f2(a, b), f2(1.f, 0.0625f), f2(-8388608.0f, -524288.0f));
-  q23 = __ffma2_rn(f2(c, d), f2(0.00390625f, 0.000244140625f), f2(-32768.0f, -2048.0f));
+__device__ __forceinline__ bool spin_geq(const uint32_t* cnt, uint32_t target, uint64_t timeout_ns) {
+  if (ld_acquire_u32(cnt) >= target) return true;
+  return spin_geq_slow(cnt, target, timeout_ns);
 }
 
 constexpr uint32_t MAGIC16 = 0x64006400u;   // fp16 pair (1024, 1024): codes OR-ed into the low mantissa bits
-
-// f32 += f16 * f16 on the low (or high) halves of two 32-bit registers; the product is exact in fp32.
-__device__ __forceinline__ float fmix_lo(uint32_t a, uint32_t b, float c) {
-  asm("{\n .reg .f16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
-      " fma.rn.f32.f16 %0, al, bl, %0;\n}"
-      : "+f"(c)
-      : "r"(a), "r"(b));
-  return c;
-}
-__device__ __forceinline__ float fmix_hi(uint32_t a, uint32_t b, float c) {
-  asm("{\n .reg .f16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
-      " fma.rn.f32.f16 %0, ah, bh, %0;\n}"
-      : "+f"(c)
-      : "r"(a), "r"(b));
-  return c;
-}
 
 // Code pairs as fp16 (1024 + code) values, two per 32-bit register, in the column pairing (k, 4+k) of an
 // 8-column block. int4 word w (column n in bits 4n..4n+3): v[0] = (q0, q4), v[2] = (q2, q6) hold 1024 + q;

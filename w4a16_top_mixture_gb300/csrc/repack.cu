@@ -13,14 +13,16 @@ __device__ __forceinline__ uint32_t sb_pair(const uint16_t* s, const uint16_t* b
   return (uint32_t)s[i] | ((uint32_t)b[i] << 16);
 }
 
-// int8 rows: n_rows rows of `cols` codes -> permuted codes at dst + r*stride + base, (s,b) pairs after.
+// int8 rows: n_rows rows of `cols` codes -> codes at dst + r*stride + code_off, (s,b) pairs at sb_off. permute 1:
+// lane-interleaved 16-byte halves of 32-column chunks with the in-block order (moe_int8_perm); 2: the in-block
+// order only (columns 0 1 4 5 2 3 6 7 of every 8-byte block).
 __global__ void k_repack_int8_rows(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s,
                                    const uint16_t* __restrict__ b, uint8_t* __restrict__ dst, int n_rows,
                                    int cols, size_t stride, size_t code_off, size_t sb_off, int permute, int LW) {
   size_t n = (size_t)n_rows * cols;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
     int r = (int)(i / cols), j = (int)(i % cols);
-    int pos = permute ? moe_int8_perm(j, LW) : j;
+    int pos = permute == 1 ? moe_int8_perm(j, LW) : permute == 2 ? moe_int8_block_col(j) : j;
     uint8_t* row = dst + (size_t)r * stride;
     row[code_off + pos] = q[i];
     if ((j & 63) == 0) {
@@ -30,26 +32,29 @@ __global__ void k_repack_int8_rows(const uint8_t* __restrict__ q, const uint16_t
   }
 }
 
-// int4 rows (packed bytes copied as they are): n_rows rows of cols/2 bytes.
+// int4 rows: n_rows rows of cols/2 bytes, one 32-bit word (8 codes) per thread, re-laid from the canonical
+// packing (code n at bits 4n) into the decode layout (moe_int4_word).
 __global__ void k_repack_int4_rows(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s,
                                    const uint16_t* __restrict__ b, uint8_t* __restrict__ dst, int n_rows,
                                    int cols, size_t stride, size_t code_off, size_t sb_off) {
-  size_t nb = (size_t)n_rows * (cols / 2);
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nb; i += (size_t)gridDim.x * blockDim.x) {
-    int r = (int)(i / (cols / 2)), jb = (int)(i % (cols / 2));
+  const int wpr = cols / 8;   // words per row
+  size_t nw = (size_t)n_rows * wpr;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nw; i += (size_t)gridDim.x * blockDim.x) {
+    int r = (int)(i / wpr), jw = (int)(i % wpr);
     uint8_t* row = dst + (size_t)r * stride;
-    row[code_off + jb] = q[i];
-    if ((jb & 31) == 0) {
-      size_t g = (size_t)r * (cols / 64) + jb / 32;
-      *reinterpret_cast<uint32_t*>(row + sb_off + (jb / 32) * 4) = sb_pair(s, b, g);
+    *reinterpret_cast<uint32_t*>(row + code_off + (size_t)jw * 4) = moe_int4_word(reinterpret_cast<const uint32_t*>(q)[i]);
+    if ((jw & 7) == 0) {
+      size_t g = (size_t)r * (cols / 64) + jw / 8;
+      *reinterpret_cast<uint32_t*>(row + sb_off + (jw / 8) * 4) = sb_pair(s, b, g);
     }
   }
 }
 
 // ---------------------------------------------------------------- debug dequantisation
 // which: 0 router, 1 expert gate, 2 expert up, 3 expert down, 4 shared gate, 5 shared up, 6 shared down.
-// Output row-major in the canonical orientation. Every element goes through the forward kernels' unpack
-// helpers and then w = fma(s, q, b) in fp32 (exactly the correctly rounded s*q + b).
+// Output row-major in the canonical orientation. Each element's code is read back from its place in the decode
+// layout (the positions the forward kernels' dot products pair with the activations) and dequantised as
+// w = fma(s, q, b) in fp32, which is exactly the correctly rounded s*q + b.
 __global__ void k_debug_dequant(const uint8_t* __restrict__ base, MoeLayout L, int which, int index,
                                 float* __restrict__ out) {
   int rows, cols;
@@ -65,26 +70,28 @@ __global__ void k_debug_dequant(const uint8_t* __restrict__ base, MoeLayout L, i
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
     int r = (int)(i / (cols / 8));
     int c8 = (int)(i % (cols / 8)) * 8;
-    float v[8];
-    if (which == 0 || which == 4 || which == 5) {
+    int qv[8];
+    const uint8_t* sbp;
+    if (which == 0 || which == 4 || which == 5 || which == 6) {
       const uint8_t* row;
-      size_t sb_off;
-      if (which == 0) { row = base + (size_t)r * L.RR; sb_off = L.H; }
-      else { row = base + (size_t)r * L.SU + (which == 5 ? L.H : 0); sb_off = 2 * (size_t)L.H - (which == 5 ? L.H : 0) + (which == 5 ? (size_t)L.GB * 4 : 0); }
-      // the 8-byte block of columns c8..c8+7 starts at the permuted position of column c8
-      const uint8_t* blk = row + moe_int8_perm(c8, L.LW);
-      uint32_t pr[4];
-      int8_block_pairs(*reinterpret_cast<const uint32_t*>(blk), *reinterpret_cast<const uint32_t*>(blk + 4), pr);
-      float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + sb_off + (c8 / 64) * 4));
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = h2f(pr[k]);   // (1024 + c_k, 1024 + c_{4+k}) exactly
-        v[k] = __fmaf_rn(sb.x, f.x - 1024.0f, sb.y);
-        v[4 + k] = __fmaf_rn(sb.x, f.y - 1024.0f, sb.y);
+      const uint8_t* blk;
+      if (which == 6) {
+        row = base + (size_t)r * L.SDR;
+        sbp = row + L.Is;
+        blk = row + c8;                                       // in-block order only
+      } else {
+        if (which == 0) { row = base + (size_t)r * L.RR; sbp = row + L.H; }
+        else {
+          const uint8_t* unit = base + (size_t)r * L.SU;
+          row = unit + (which == 5 ? L.H : 0);
+          sbp = unit + 2 * (size_t)L.H + (which == 5 ? (size_t)L.GB * 4 : 0);
+        }
+        blk = row + moe_int8_perm(c8, L.LW);                  // the block of columns c8..c8+7
       }
-    } else if (which >= 1 && which <= 3) {
+      for (int k = 0; k < 8; ++k) qv[k] = blk[moe_int8_block_pos(k)];
+    } else {
       // int4 rows: expert gate / up (units of gate row | up row | pairs) or down (row | pairs)
       const uint8_t* row;
-      const uint8_t* sbp;
       if (which == 3) {
         row = base + ((size_t)index * L.H + r) * L.DR;
         sbp = row + L.I / 2;
@@ -93,31 +100,12 @@ __global__ void k_debug_dequant(const uint8_t* __restrict__ base, MoeLayout L, i
         row = unit + (which == 2 ? L.H / 2 : 0);
         sbp = unit + (size_t)L.H + (which == 2 ? (size_t)L.GB * 4 : 0);
       }
-      uint32_t w = *reinterpret_cast<const uint32_t*>(row + c8 / 2);
-      uint32_t pr[4];
-      int4_word_pairs(w, pr);
-      float2 sb = h2f(*reinterpret_cast<const uint32_t*>(sbp + (c8 / 64) * 4));
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = h2f(pr[k]);   // 1024 + q (k even) or 1024 + 16 q (k odd), exactly
-        const float sc = (k & 1) ? 0.0625f : 1.0f;
-        v[k] = __fmaf_rn(sb.x, (f.x - 1024.0f) * sc, sb.y);
-        v[4 + k] = __fmaf_rn(sb.x, (f.y - 1024.0f) * sc, sb.y);
-      }
-    } else {
-      const uint8_t* row = base + (size_t)r * L.SDR;
-      uint32_t w0 = *reinterpret_cast<const uint32_t*>(row + c8);
-      uint32_t w1 = *reinterpret_cast<const uint32_t*>(row + c8 + 4);
-      float2 q[4];
-      unpack_int8_word(w0, q[0], q[1]);
-      unpack_int8_word(w1, q[2], q[3]);
-      float2 sb = h2f(*reinterpret_cast<const uint32_t*>(row + L.Is + (c8 / 64) * 4));
-      for (int k = 0; k < 4; ++k) {
-        v[2 * k] = __fmaf_rn(sb.x, q[k].x, sb.y);
-        v[2 * k + 1] = __fmaf_rn(sb.x, q[k].y, sb.y);
-      }
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(row + c8 / 2);
+      for (int k = 0; k < 8; ++k) qv[k] = (int)((w >> moe_int4_shift(k)) & 0xFu);
     }
+    const float2 sb = h2f(*reinterpret_cast<const uint32_t*>(sbp + (c8 / 64) * 4));
     float* o = out + (size_t)r * cols + c8;
-    for (int k = 0; k < 8; ++k) o[k] = v[k];
+    for (int k = 0; k < 8; ++k) o[k] = __fmaf_rn(sb.x, (float)qv[k], sb.y);
   }
 }
 
@@ -138,17 +126,17 @@ cudaError_t repack_all(const RepackSrc& w, const MoeLayout& L, const RepackDst& 
                                                                 H, L.SU, 0, 2 * (size_t)H, 1, L.LW);
   k_repack_int8_rows<<<grid_for((size_t)Is * H), 256, 0, st>>>(w.sh_up_q, w.sh_up_s, w.sh_up_b, d.sh_gu, Is, H,
                                                                 L.SU, H, 2 * (size_t)H + (size_t)L.GB * 4, 1, L.LW);
-  // shared down rows (natural order)
+  // shared down rows (in-block order)
   k_repack_int8_rows<<<grid_for((size_t)H * Is), 256, 0, st>>>(w.sh_down_q, w.sh_down_s, w.sh_down_b, d.sh_dn, H,
-                                                                Is, L.SDR, 0, Is, 0, L.LW);
+                                                                Is, L.SDR, 0, Is, 2, L.LW);
   // expert gate/up units: rows of all experts are consecutive (e*I + i)
-  k_repack_int4_rows<<<grid_for((size_t)E * I * H / 2), 256, 0, st>>>(w.exp_gate_q, w.exp_gate_s, w.exp_gate_b,
+  k_repack_int4_rows<<<grid_for((size_t)E * I * H / 8), 256, 0, st>>>(w.exp_gate_q, w.exp_gate_s, w.exp_gate_b,
                                                                        d.ex_gu, E * I, H, L.EU, 0, H);
-  k_repack_int4_rows<<<grid_for((size_t)E * I * H / 2), 256, 0, st>>>(w.exp_up_q, w.exp_up_s, w.exp_up_b, d.ex_gu,
+  k_repack_int4_rows<<<grid_for((size_t)E * I * H / 8), 256, 0, st>>>(w.exp_up_q, w.exp_up_s, w.exp_up_b, d.ex_gu,
                                                                        E * I, H, L.EU, H / 2,
                                                                        (size_t)H + (size_t)L.GB * 4);
   // expert down rows: rows of all experts are consecutive (e*H + r)
-  k_repack_int4_rows<<<grid_for((size_t)E * H * I / 2), 256, 0, st>>>(w.exp_down_q, w.exp_down_s, w.exp_down_b,
+  k_repack_int4_rows<<<grid_for((size_t)E * H * I / 8), 256, 0, st>>>(w.exp_down_q, w.exp_down_s, w.exp_down_b,
                                                                        d.ex_dn, E * H, I, L.DR, 0, I / 2);
   return cudaGetLastError();
 }
