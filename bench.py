@@ -17,7 +17,6 @@ import json
 import os
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -193,13 +192,15 @@ print(json.dumps({{"tokens": n, "seconds": time.perf_counter() - t0}}))
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "tokens_per_step": 1},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "cpu_count": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def _time_graph(fn, reps=10, per=20):
-    """Device time per call of fn (CUDA events around replays of a graph of `per` calls), after warm-up."""
+    """Device time per call of fn: CUDA events around each of `reps` replays of a graph of `per` calls, after
+    warm-up. Returns (median, list of per-replay times), microseconds per call."""
     import torch
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -213,67 +214,92 @@ def _time_graph(fn, reps=10, per=20):
             fn()
     g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    ts = []
     for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
         g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / (reps * per)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / per)
+    return float(np.median(ts)), ts
 
 
-def extra_configs(blocks, X):
-    """Throughput of the other block configurations (tokens/s and us per block), each on synthetic inputs of its
-    shape; inputs are device-resident, times are device times of graph-replayed calls."""
+def _roofline_entry(cfg, U, T, us, peak):
+    """Algorithmic bytes of one call (router, shared expert, U unique experts), achieved GB/s and fractions."""
+    b = synth.unique_weight_bytes(cfg, U)
+    gbs = b / (us * 1e-6) / 1e9
+    return {"unique_experts": int(U), "algorithmic_bytes": int(b), "achieved_gbs": gbs, "frac": gbs / peak,
+            "frac_of_8tbs": gbs / 8000.0, "tokens": T}
+
+
+def extra_configs(stk, blocks, X, peak):
+    """The other block configurations, each on seeded synthetic inputs of its shape (device-resident; times are
+    device times). Unique experts U come from the call's own routing record; roofline fractions are against
+    the measured HBM peak (frac) and against 8 TB/s (frac_of_8tbs)."""
     import torch
     from w4a16_top_mixture_gb300 import lib
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from _cases import make_case   # seeded inputs that respect the routing-gap rule (generators only)
     out = {}
 
     def dev(x):
         return torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
 
+    def unique(b, T):
+        return len(np.unique(b.last_routing(T)["ids"].cpu().numpy()))
+
     # tiny block, T = 1
-    w, x = make_case(synth.TINY, 1, 5)
-    b = lib.MoeBlock.from_config(synth.TINY, max_tokens=1)
-    b.load_weights(w)
-    xd, od = dev(x), torch.empty((1, synth.TINY.hidden), dtype=torch.float16, device="cuda")
-    us = _time_graph(lambda: b.forward(xd, od))
-    out["tiny_T1"] = {"us_per_block": us, "tokens_per_s": 1e6 / us, "note": "L2-resident (one tiny layer)"}
+    cfg = synth.TINY
+    b = lib.MoeBlock.from_config(cfg, max_tokens=1)
+    b.load_weights(synth.gen_layer(cfg, 5))
+    xd, od = dev(synth.gen_x(cfg, 1, 5)), torch.empty((1, cfg.hidden), dtype=torch.float16, device="cuda")
+    us, _ = _time_graph(lambda: b.forward(xd, od))
+    out["tiny_T1"] = {"us_per_block": us, "tokens_per_s": 1e6 / us, "note": "L2-resident (one tiny layer)",
+                      **_roofline_entry(cfg, unique(b, 1), 1, us, peak)}
     b.close()
     # production block, T = 16, Zipf(1.1) routing, 4 layers rotated
     cfg = synth.PROD
     bs, xs = [], []
     for l in range(4):
-        w, x = make_case(cfg, 16, 42 + l, routing="zipf")
+        x = synth.gen_x(cfg, 16, 42 + l)
+        w = synth.gen_layer(cfg, 42 + l)
+        w["router_q"], w["router_s"], w["router_b"] = synth.zipf_router(cfg, x, 42 + l)
         b = lib.MoeBlock.from_config(cfg, max_tokens=16)
         b.load_weights(w)
         bs.append(b)
         xs.append(dev(x))
     od = torch.empty((16, cfg.hidden), dtype=torch.float16, device="cuda")
+    Us = []
+    for b, x in zip(bs, xs):
+        b.forward(x, od)
+        torch.cuda.synchronize()
+        Us.append(unique(b, 16))
     it = [0]
 
     def step16():
         i = it[0] % 4
         it[0] += 1
         bs[i].forward(xs[i], od)
-    us = _time_graph(step16)
-    out["batched_T16_zipf"] = {"us_per_block": us, "tokens_per_s": 16e6 / us}
+    us, _ = _time_graph(step16)
+    U = float(np.mean(Us))
+    out["batched_T16_zipf"] = {"us_per_block": us, "tokens_per_s": 16e6 / us, "U_per_layer": Us,
+                               **_roofline_entry(cfg, U, 16, us, peak)}
     for b in bs:
         b.close()
-    # 40 stacked layers with RMSNorm + residual, T = 1: one token through every layer per call
+    # 40 stacked layers with RMSNorm + residual, T = 1: one moe_stack_forward call (one chain of launches)
+    # per token through all layers
     h = [X[0:1].clone(), torch.empty_like(X[0:1])]
-
-    def stack():
-        for l, b in enumerate(blocks):
-            b.forward_residual(h[l & 1], h[(l + 1) & 1])
-    us = _time_graph(stack, reps=5, per=5)
-    out["stack_T1"] = {"layers": len(blocks), "us_per_token": us, "us_per_block": us / len(blocks),
-                       "tokens_per_s": 1e6 / us}
+    us, _ = _time_graph(lambda: stk.forward(h[0], h[1]), reps=10, per=5)
+    nl = stk.n_layers
+    ent = _roofline_entry(cfg, cfg.top_k, 1, us / nl, peak)
+    ent["algorithmic_bytes_per_call"] = ent["algorithmic_bytes"] * nl
+    out["stack_T1"] = {"layers": nl, "us_per_token": us, "us_per_block": us / nl, "tokens_per_s": 1e6 / us,
+                       "api": "moe_stack_forward", **ent}
     # prompt chunk T = 512, uniform and Zipf routing (tcgen05 grouped-GEMM path)
     for routing, seed in (("uniform", 553), ("zipf", 42)):
-        w, x = make_case(cfg, 512, seed, routing=routing)
+        x = synth.gen_x(cfg, 512, seed)
+        w = synth.gen_layer(cfg, seed)
+        if routing == "zipf":
+            w["router_q"], w["router_s"], w["router_b"] = synth.zipf_router(cfg, x, seed)
         b = lib.MoeBlock.from_config(cfg, max_tokens=512)
         b.load_weights(w)
         xd, od = dev(x), torch.empty((512, cfg.hidden), dtype=torch.float16, device="cuda")
@@ -289,7 +315,11 @@ def extra_configs(blocks, X):
             if r >= 3:
                 ts.append(e0.elapsed_time(e1) * 1e3)
         us = float(np.median(ts))
-        out[f"chunk_T512_{routing}"] = {"us_per_block": us, "tokens_per_s": 512e6 / us}
+        U = unique(b, 512)
+        ent = _roofline_entry(cfg, U, 512, us, peak)
+        flops = 2.0 * 512 * cfg.top_k * 3 * cfg.hidden * cfg.expert_inter   # routed work, 2 flops a weight a token
+        ent["routed_tflops"] = flops / (us * 1e-6) / 1e12
+        out[f"chunk_T512_{routing}"] = {"us_per_block": us, "tokens_per_s": 512e6 / us, **ent}
         b.close()
         del flush
     return out
@@ -309,17 +339,17 @@ def run_ours(args):
     build.build()
     cfg = synth.PROD
     NL = args.layers
-    blocks = []
+    # The layers live in one stack (it serves the stacked configuration as a whole); the headline steps call
+    # its layers one at a time through their own block handles.
+    stk = lib.MoeStack(cfg, NL, max_tokens=1, eps=1e-6)
     for l in range(NL):
-        w = synth.gen_layer(cfg, rank_seed(rank), l, with_gamma=True)   # gamma serves the stack config
-        b = lib.MoeBlock.from_config(cfg, max_tokens=1)
-        b.load_weights(w)                      # host arrays: copied and repacked by the library
-        blocks.append(b)
-        del w
+        stk.load_layer(l, synth.gen_layer(cfg, rank_seed(rank), l, with_gamma=True))   # host arrays: repacked
+    blocks = [lib.MoeBlock.borrow(stk, l) for l in range(NL)]
     pool = 4096
     xh = synth.gen_x_fast(cfg, pool, 77 + rank)
     X = torch.from_numpy(xh.view(np.int16)).cuda().view(torch.float16)
     OUT = torch.empty_like(X)
+
     def step(i):
         b = blocks[i % NL]
         j = i % pool
@@ -331,7 +361,7 @@ def run_ours(args):
         for i in range(args.warmup):
             step(i)
     torch.cuda.synchronize()
-    s, f = blocks[0].status()
+    s, f = stk.status()
     if s != 0:
         raise RuntimeError(f"device status {s} flags {f:#x}")
 
@@ -339,6 +369,7 @@ def run_ours(args):
     # leave the GPU idle between the short decode kernels.
     K = args.steps
     S = min(K, 200)
+
     def capture(n, base):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=side):
@@ -368,11 +399,20 @@ def run_ours(args):
     elapsed_ms = t_start.elapsed_time(t_end)
     launches = K * launches_per_step
     kern_ms = elapsed_ms / K            # per launch, including the gap between graph nodes
-    for b in blocks[:1]:
-        s, f = b.status()
-        if s != 0:
-            raise RuntimeError(f"device status {s} flags {f:#x}")
+    s, f = stk.status()
+    if s != 0:
+        raise RuntimeError(f"device status {s} flags {f:#x}")
     elapsed_ms = max_over_ranks(elapsed_ms)
+    # a longer record of the same step: the median over 50 replays of a 200-step graph (extra field)
+    g_med = capture(200, args.warmup + K)
+    reps = []
+    for _ in range(50):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g_med.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        reps.append(e0.elapsed_time(e1) * 1e3 / 200)
 
     # end-to-end through the C ABI with host buffers (pinned), copies inside the timed region
     Ke = min(K, 2000)
@@ -404,24 +444,26 @@ def run_ours(args):
                        "timing": f"CUDA graphs of {S} steps replayed; CUDA events around the replays",
                        "parallelism": f"replicas x{world}", "weights": "int4/int8 g64 affine, fp16 activations"},
             "us_per_block": kern_ms * 1e3,
+            "us_per_block_median_50x200": float(np.median(reps)),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": tr, "peak_kind": kind,
+                         "frac_of_8tbs": achieved / 8000.0,
                          "algorithmic_bytes_per_launch": bytes_call,
                          "kernel": "k_decode1 (fused single-token decode kernel, one launch per step)"},
-            "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": cpu_v, "unit": "tokens/s", "cores": 1, "cpu_count": os.cpu_count(),
+                             "kind": "oracle",
                              "sample": f"{cpu_d['tokens']} T=1 tokens through one production block in "
                                        f"{cpu_d['seconds']:.1f} s, single-threaded float64 numpy"},
             "e2e": {"value": whole_job_value(world, Ke, e2e_s * 1e3), "unit": "tokens/s", "h2d_bytes_per_step": 2 * cfg.hidden,
                     "d2h_bytes_per_step": 2 * cfg.hidden,
-                    "how": "moe_block_forward_host: pinned x -> device, forward, out -> host, stream sync, per step"},
+                    "how": "moe_block_forward_host: pinned x -> device, forward, out -> host, status word, stream sync, per step"},
             "gpu_launches": launches,
             "clocks": clk.summary(),
         }
         if not args.no_extras:
-            line["configs"] = extra_configs(blocks, X)
+            line["configs"] = extra_configs(stk, blocks, X, peak)
         print(json.dumps(line), flush=True)
-    for b in blocks:
-        b.close()
+    stk.close()
     if world > 1:
         dist.destroy_process_group()
 

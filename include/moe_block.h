@@ -102,10 +102,46 @@ MOE_API int moe_block_forward_host(moe_block_t *blk, const void *x_host, void *o
  * rms_gamma loaded. h_in and h_out fp16 device [T][H]; they may alias. */
 MOE_API int moe_block_forward_residual(moe_block_t *blk, const void *h_in, void *h_out, int T, float eps, void *stream);
 
-/* Synchronises the handle's device work and returns MOE_OK or MOE_ERR_DEVICE_TIMEOUT if a bounded
- * device-side wait ran out in any earlier call (the handle's device state is then reset, so the next call
- * starts clean). *flags (may be NULL) receives the raw device error bits. */
+/* Waits for the stream of the handle's last forward call (that stream must still exist; work replayed from a
+ * CUDA graph on another stream must be synchronised by the caller first), then returns MOE_OK, or
+ * MOE_ERR_DEVICE_TIMEOUT if a bounded device-side wait ran out in any earlier call (the handle's device state
+ * is then reset, so the next call starts clean). *flags (may be NULL) receives the raw device error bits. */
 MOE_API int moe_block_get_status(moe_block_t *blk, uint32_t *flags);
+
+/* ---- stacked decoder layers (notebook section 7: the decoder layer wraps the MoE block in RMSNorm and a
+ * residual add; TensorFold #3239, "What this changes": staged references compare each layer's local error
+ * with the error chained through the stack) ----
+ *
+ * A stack holds n_layers blocks of one shape, each with its own weights and RMSNorm gamma, and runs
+ *   h_{l+1} = h_l + block_l(RMSNorm_l(h_l)),  l = 0 .. n_layers-1,   RMSNorm(h) = h / sqrt(mean(h^2) + eps) * gamma
+ * on fp16 hidden states: h_in = h_0, h_out = h_{n_layers}; between layers the residual stream is fp16. */
+typedef struct moe_stack moe_stack_t;   /* opaque, owned by the library */
+
+/* n_layers >= 1 blocks of shape *cfg (every layer allocates its own weight store and scratch, as
+ * moe_block_create does), plus two [max_tokens][H] fp16 buffers for the residual stream. eps > 0. */
+MOE_API int moe_stack_create(const moe_block_config_t *cfg, int n_layers, float eps, moe_stack_t **out);
+
+/* Weights of layer `layer` (0-based) in the canonical layout of moe_block_load_weights; rms_gamma is
+ * required. Synchronises `stream`; the caller may free its buffers on return. */
+MOE_API int moe_stack_load_layer(moe_stack_t *stk, int layer, const moe_block_weights_t *w, int weights_on_device,
+                                 void *stream);
+
+/* h_out[T][H] = the stack applied to h_in[T][H] (fp16 device buffers, 16-byte aligned; h_out may alias h_in
+ * when T <= 16 or n_layers > 1). per_layer_out: NULL, or fp16 device [n_layers][T][H] that receives h_{l+1}
+ * for every layer l (the per-layer record of the staged-reference method). Every layer must be loaded. The
+ * layers are issued back to back on `stream` as programmatic-dependent launches (at T = 1 the next layer's CTAs
+ * become resident and load their weight-only rows while the current layer runs); no host synchronisation and
+ * no allocation. */
+MOE_API int moe_stack_forward(moe_stack_t *stk, const void *h_in, void *h_out, int T, void *per_layer_out,
+                              void *stream);
+
+/* moe_block_get_status over every layer (flags: the OR of their error bits). */
+MOE_API int moe_stack_get_status(moe_stack_t *stk, uint32_t *flags);
+
+/* The handle of layer `layer` (owned by the stack; for the per-block test hooks), or NULL. */
+MOE_API moe_block_t *moe_stack_layer(moe_stack_t *stk, int layer);
+
+MOE_API void moe_stack_destroy(moe_stack_t *stk);
 
 MOE_API void moe_block_destroy(moe_block_t *blk);
 MOE_API const char *moe_block_strerror(int status);

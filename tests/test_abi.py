@@ -71,3 +71,22 @@ def test_binding_without_library_raises(tmp_path):
             lib.load_library(str(tmp_path / "missing.so"))
     finally:
         lib._LIB = saved
+
+
+def test_stack_invalid_arguments_without_device(L):
+    import torch
+    h = ctypes.c_void_p()
+    cfg = lib.Config(2048, 256, 8, 512, 512, 64, 1)
+    assert L.moe_stack_create(None, 4, 1e-6, ctypes.byref(h)) == -1
+    assert L.moe_stack_create(ctypes.byref(cfg), 0, 1e-6, ctypes.byref(h)) == -1
+    assert L.moe_stack_create(ctypes.byref(cfg), 4, 0.0, ctypes.byref(h)) == -1
+    assert L.moe_stack_create(ctypes.byref(cfg), 4, 1e-6, None) == -1
+    bad = lib.Config(2048, 256, 8, 512, 512, 32, 1)
+    assert L.moe_stack_create(ctypes.byref(bad), 4, 1e-6, ctypes.byref(h)) == -2
+    if not torch.cuda.is_available():
+        assert L.moe_stack_create(ctypes.byref(cfg), 4, 1e-6, ctypes.byref(h)) == -6
+        assert h.value is None
+    assert L.moe_stack_forward(None, None, None, 1, None, None) == -1
+    assert L.moe_stack_load_layer(None, 0, None, 0, None) == -1
+    assert L.moe_stack_get_status(None, None) == -1
+    assert L.moe_stack_layer(None, 0) is None

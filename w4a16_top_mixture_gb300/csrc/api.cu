@@ -436,3 +436,107 @@ extern "C" int moe_block_debug_set_trace(moe_block_t* b, void* trace_device) {
 }
 
 extern "C" int moe_block_last_launch_count(moe_block_t* b) { return b ? b->last_launches : 0; }
+
+// ---------------------------------------------------------------- stacked decoder layers
+
+struct moe_stack {
+  moe_block_config_t cfg;
+  int n_layers = 0;
+  float eps = 0.f;
+  moe_block** layers = nullptr;
+  bool* loaded = nullptr;
+  uint16_t* buf[2] = {nullptr, nullptr};   // the residual stream between layers, [max_tokens][H] fp16 each
+};
+
+extern "C" void moe_stack_destroy(moe_stack_t* s) {
+  if (!s) return;
+  if (s->layers)
+    for (int l = 0; l < s->n_layers; ++l) moe_block_destroy(s->layers[l]);
+  cudaFree(s->buf[0]);
+  cudaFree(s->buf[1]);
+  delete[] s->layers;
+  delete[] s->loaded;
+  delete s;
+}
+
+extern "C" int moe_stack_create(const moe_block_config_t* cfg, int n_layers, float eps, moe_stack_t** out) {
+  if (!cfg || !out || n_layers < 1 || n_layers > 4096 || !(eps > 0.f)) return MOE_ERR_INVALID_ARG;
+  {
+    const int st = check_config(*cfg);
+    if (st != MOE_OK) return st;
+  }
+  moe_stack* s = new (std::nothrow) moe_stack;
+  if (!s) return MOE_ERR_CUDA;
+  s->cfg = *cfg;
+  s->eps = eps;
+  s->layers = new (std::nothrow) moe_block*[n_layers]();
+  s->loaded = new (std::nothrow) bool[n_layers]();
+  if (!s->layers || !s->loaded) { moe_stack_destroy(s); return MOE_ERR_CUDA; }
+  for (int l = 0; l < n_layers; ++l) {
+    const int st = moe_block_create(cfg, &s->layers[l]);
+    if (st != MOE_OK) { s->n_layers = l; moe_stack_destroy(s); return st; }
+    s->n_layers = l + 1;
+  }
+  const size_t bytes = (size_t)cfg->max_tokens * cfg->hidden * 2;
+  cudaError_t e = cudaMalloc(&s->buf[0], bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&s->buf[1], bytes);
+  if (e != cudaSuccess) { moe_stack_destroy(s); return cuda_fail(e, "moe_stack_create"); }
+  *out = s;
+  return MOE_OK;
+}
+
+extern "C" int moe_stack_load_layer(moe_stack_t* s, int layer, const moe_block_weights_t* w, int on_device,
+                                    void* stream) {
+  if (!s || !w || layer < 0 || layer >= s->n_layers || !w->rms_gamma) return MOE_ERR_INVALID_ARG;
+  const int st = moe_block_load_weights(s->layers[layer], w, on_device, stream);
+  if (st == MOE_OK) s->loaded[layer] = true;
+  return st;
+}
+
+extern "C" int moe_stack_forward(moe_stack_t* s, const void* h_in, void* h_out, int T, void* per_layer_out,
+                                 void* stream) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > s->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!h_in || !h_out || !aligned16(h_in) || !aligned16(h_out)) return MOE_ERR_INVALID_ARG;
+  if (per_layer_out && !aligned16(per_layer_out)) return MOE_ERR_INVALID_ARG;
+  // the prompt-chunk path reads its whole input before it writes, but not within one kernel: a single layer
+  // may not alias there
+  if (s->n_layers == 1 && T > DEC_TMAX && h_in == h_out) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < s->n_layers; ++l)
+    if (!s->loaded[l]) return MOE_ERR_NOT_LOADED;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t plane = (size_t)T * s->cfg.hidden;
+  const uint16_t* in = (const uint16_t*)h_in;
+  for (int l = 0; l < s->n_layers; ++l) {
+    moe_block* b = s->layers[l];
+    uint16_t* out = l == s->n_layers - 1 ? (uint16_t*)h_out : s->buf[l & 1];
+    uint16_t* rec = per_layer_out ? (uint16_t*)per_layer_out + (size_t)l * plane : nullptr;
+    // the decode kernels write the per-layer record themselves; the chunk path gets a copy
+    const bool dec = T <= DEC_TMAX || !b->chunk;
+    int r = run_forward(b, in, out, T, b->gamma, s->eps, st, dec ? rec : nullptr);
+    if (r != MOE_OK) return r;
+    if (rec && !dec) CK(cudaMemcpyAsync(rec, out, plane * 2, cudaMemcpyDeviceToDevice, st));
+    in = out;
+  }
+  return MOE_OK;
+}
+
+extern "C" int moe_stack_get_status(moe_stack_t* s, uint32_t* flags) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  uint32_t all = 0;
+  int result = MOE_OK;
+  for (int l = 0; l < s->n_layers; ++l) {
+    uint32_t f = 0;
+    const int r = moe_block_get_status(s->layers[l], &f);
+    all |= f;
+    if (r != MOE_OK && result == MOE_OK) result = r;
+  }
+  if (flags) *flags = all;
+  return result;
+}
+
+extern "C" moe_block_t* moe_stack_layer(moe_stack_t* s, int layer) {
+  if (!s || layer < 0 || layer >= s->n_layers) return nullptr;
+  return s->layers[layer];
+}

@@ -687,7 +687,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
         for (int j = 0; j < K; ++j) acc += ctl->wts[t][j] * yv[(size_t)ctl->tok_pair[t][j] * nrow + rr];
         float v = acc + ctl->sg[t] * shs[t * nrow + rr];
         if (a.gamma) v += __half2float(__ushort_as_half(a.x[(size_t)t * H + r0 + rr]));
-        a.out[(size_t)t * H + r0 + rr] = __half_as_ushort(__float2half_rn(v));
+        const uint16_t o = __half_as_ushort(__float2half_rn(v));
+        a.out[(size_t)t * H + r0 + rr] = o;
+        if (a.out2) a.out2[(size_t)t * H + r0 + rr] = o;
       }
     named_bar(BAR_C, CT);
   }

@@ -23,7 +23,8 @@ EXPORTS = ["moe_block_create", "moe_block_load_weights", "moe_block_forward", "m
            "moe_block_forward_residual", "moe_block_get_status", "moe_block_destroy", "moe_block_strerror",
            "moe_last_cuda_error", "moe_block_debug_dequant", "moe_block_debug_last_routing",
            "moe_block_debug_set_wait", "moe_block_debug_set_trace", "moe_block_last_launch_count",
-           "moe_router_topk_noalloc", "moe_debug_decode_plan"]
+           "moe_router_topk_noalloc", "moe_debug_decode_plan", "moe_stack_create", "moe_stack_load_layer",
+           "moe_stack_forward", "moe_stack_get_status", "moe_stack_layer", "moe_stack_destroy"]
 
 
 class MoeError(RuntimeError):
@@ -78,6 +79,14 @@ def load_library(path: str = LIB_PATH):
     lib.moe_block_debug_set_trace.argtypes = [vp, vp]
     lib.moe_router_topk_noalloc.argtypes = [vp, vp, vp, i, i, i, vp, i, vp, vp, vp, vp]
     lib.moe_debug_decode_plan.argtypes = [ctypes.POINTER(Config), i, i, i, ctypes.POINTER(ctypes.c_int32)]
+    lib.moe_stack_create.argtypes = [ctypes.POINTER(Config), i, ctypes.c_float, ctypes.POINTER(vp)]
+    lib.moe_stack_load_layer.argtypes = [vp, i, ctypes.POINTER(Weights), i, vp]
+    lib.moe_stack_forward.argtypes = [vp, vp, vp, i, vp, vp]
+    lib.moe_stack_get_status.argtypes = [vp, ctypes.POINTER(u32)]
+    lib.moe_stack_layer.argtypes = [vp, i]
+    lib.moe_stack_layer.restype = vp
+    lib.moe_stack_destroy.argtypes = [vp]
+    lib.moe_stack_destroy.restype = None
     for n in EXPORTS:
         if not hasattr(lib, n):
             raise RuntimeError(f"{path} does not export {n}")
@@ -128,6 +137,23 @@ class MoeBlock:
     def from_config(cls, cfg, max_tokens=16):
         return cls(cfg.hidden, cfg.n_experts, cfg.top_k, cfg.expert_inter, cfg.shared_inter, max_tokens)
 
+    @classmethod
+    def borrow(cls, stack, layer):
+        """The block handle of one layer of a MoeStack (owned by the stack: close() leaves it alone)."""
+        b = cls.__new__(cls)
+        b.lib = stack.lib
+        b.cfg = stack.cfg
+        b.h = None
+        b._borrowed = ctypes.c_void_p(stack.lib.moe_stack_layer(stack.h, int(layer)))
+        b.hidden, b.n_experts, b.top_k = stack.cfg.hidden, stack.cfg.n_experts, stack.cfg.top_k
+        b.max_tokens = stack.cfg.max_tokens
+        b._stack = stack
+        return b
+
+    @property
+    def handle(self):
+        return self.h if self.h is not None else getattr(self, "_borrowed", None)
+
     def close(self):
         if getattr(self, "h", None):
             self.lib.moe_block_destroy(self.h)
@@ -141,31 +167,8 @@ class MoeBlock:
 
     def load_weights(self, w: dict, stream=None):
         """w: canonical arrays (numpy on the host, or torch tensors on the device; fp16 as float16/uint16)."""
-        import torch
-        keep = []
-        on_dev = None
-        W = Weights()
-        for n in WEIGHT_FIELDS:
-            a = w.get(n)
-            if a is None:
-                continue
-            if isinstance(a, np.ndarray):
-                a = np.ascontiguousarray(a)
-                if on_dev is None:
-                    on_dev = False
-                if on_dev:
-                    raise ValueError("mix of host and device weights")
-                keep.append(a)
-                setattr(W, n, a.ctypes.data)
-            else:
-                assert isinstance(a, torch.Tensor) and a.is_cuda and a.is_contiguous()
-                if on_dev is None:
-                    on_dev = True
-                if not on_dev:
-                    raise ValueError("mix of host and device weights")
-                keep.append(a)
-                setattr(W, n, a.data_ptr())
-        _check(self.lib.moe_block_load_weights(self.h, ctypes.byref(W), int(bool(on_dev)), _stream_ptr(stream)),
+        W, keep, on_dev = _weights_struct(w)
+        _check(self.lib.moe_block_load_weights(self.handle, ctypes.byref(W), int(on_dev), _stream_ptr(stream)),
                "moe_block_load_weights")
 
     def forward(self, x, out=None, stream=None):
@@ -174,7 +177,7 @@ class MoeBlock:
         if out is None:
             out = torch.empty_like(x)
         T = x.shape[0] if x.dim() == 2 else 0
-        _check(self.lib.moe_block_forward(self.h, _ptr(x), _ptr(out), T, _stream_ptr(stream)), "moe_block_forward")
+        _check(self.lib.moe_block_forward(self.handle, _ptr(x), _ptr(out), T, _stream_ptr(stream)), "moe_block_forward")
         return out
 
     def forward_residual(self, h_in, h_out=None, eps=1e-6, stream=None):
@@ -182,7 +185,7 @@ class MoeBlock:
         assert h_in.dtype == torch.float16 and h_in.is_cuda and h_in.is_contiguous()
         if h_out is None:
             h_out = torch.empty_like(h_in)
-        _check(self.lib.moe_block_forward_residual(self.h, _ptr(h_in), _ptr(h_out), h_in.shape[0], float(eps),
+        _check(self.lib.moe_block_forward_residual(self.handle, _ptr(h_in), _ptr(h_out), h_in.shape[0], float(eps),
                                                    _stream_ptr(stream)), "moe_block_forward_residual")
         return h_out
 
@@ -193,13 +196,13 @@ class MoeBlock:
             x_host = torch.from_numpy(np.ascontiguousarray(x_host))
         if out_host is None:
             out_host = torch.empty_like(x_host)
-        _check(self.lib.moe_block_forward_host(self.h, _ptr(x_host), _ptr(out_host), x_host.shape[0],
+        _check(self.lib.moe_block_forward_host(self.handle, _ptr(x_host), _ptr(out_host), x_host.shape[0],
                                                _stream_ptr(stream)), "moe_block_forward_host")
         return out_host
 
     def status(self):
         f = ctypes.c_uint32(0)
-        s = self.lib.moe_block_get_status(self.h, ctypes.byref(f))
+        s = self.lib.moe_block_get_status(self.handle, ctypes.byref(f))
         return s, f.value
 
     def debug_dequant(self, which, index=0, stream=None):
@@ -207,7 +210,7 @@ class MoeBlock:
         H, E, I, Is = self.cfg.hidden, self.cfg.n_experts, self.cfg.expert_inter, self.cfg.shared_inter
         shape = {0: (E + 1, H), 1: (I, H), 2: (I, H), 3: (H, I), 4: (Is, H), 5: (Is, H), 6: (H, Is)}[which]
         out = torch.empty(shape, dtype=torch.float32, device="cuda")
-        _check(self.lib.moe_block_debug_dequant(self.h, which, index, _ptr(out), _stream_ptr(stream)),
+        _check(self.lib.moe_block_debug_dequant(self.handle, which, index, _ptr(out), _stream_ptr(stream)),
                "moe_block_debug_dequant")
         return out
 
@@ -218,12 +221,12 @@ class MoeBlock:
         ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
         w = torch.empty((T, K), dtype=torch.float32, device="cuda")
         sg = torch.empty((T,), dtype=torch.float32, device="cuda")
-        _check(self.lib.moe_block_debug_last_routing(self.h, T, _ptr(lg), _ptr(ids), _ptr(w), _ptr(sg),
+        _check(self.lib.moe_block_debug_last_routing(self.handle, T, _ptr(lg), _ptr(ids), _ptr(w), _ptr(sg),
                                                      _stream_ptr(stream)), "moe_block_debug_last_routing")
         return {"logits": lg, "ids": ids, "w": w, "sg": sg}
 
     def set_wait(self, timeout_us=0, skip_arrive=False):
-        _check(self.lib.moe_block_debug_set_wait(self.h, int(timeout_us), int(bool(skip_arrive))), "set_wait")
+        _check(self.lib.moe_block_debug_set_wait(self.handle, int(timeout_us), int(bool(skip_arrive))), "set_wait")
 
     def set_trace(self, buf=None):
         """buf: int64 CUDA tensor of >= 96 * SM-count entries, or None to stop tracing."""
@@ -232,10 +235,97 @@ class MoeBlock:
             sms = torch.cuda.get_device_properties(buf.device).multi_processor_count
             if buf.dtype != torch.int64 or buf.numel() < 96 * sms or not buf.is_contiguous():
                 raise ValueError(f"trace buffer must be a contiguous int64 tensor of >= {96 * sms} entries")
-        _check(self.lib.moe_block_debug_set_trace(self.h, _ptr(buf)), "set_trace")
+        _check(self.lib.moe_block_debug_set_trace(self.handle, _ptr(buf)), "set_trace")
 
     def last_launch_count(self):
-        return self.lib.moe_block_last_launch_count(self.h)
+        return self.lib.moe_block_last_launch_count(self.handle)
+
+
+def _weights_struct(w: dict):
+    """A Weights struct over the canonical arrays of w (all numpy on the host, or all torch tensors on the device),
+    with the objects that must stay alive while the library reads them, and whether they are on the device."""
+    import torch
+    keep = []
+    on_dev = None
+    W = Weights()
+    for n in WEIGHT_FIELDS:
+        a = w.get(n)
+        if a is None:
+            continue
+        if isinstance(a, np.ndarray):
+            a = np.ascontiguousarray(a)
+            if on_dev:
+                raise ValueError("mix of host and device weights")
+            on_dev = False
+            keep.append(a)
+            setattr(W, n, a.ctypes.data)
+        else:
+            assert isinstance(a, torch.Tensor) and a.is_cuda and a.is_contiguous()
+            if on_dev is False:
+                raise ValueError("mix of host and device weights")
+            on_dev = True
+            keep.append(a)
+            setattr(W, n, a.data_ptr())
+    return W, keep, bool(on_dev)
+
+
+class MoeStack:
+    """n_layers blocks of one shape, h_{l+1} = h_l + block_l(RMSNorm_l(h_l)), run as one chain of launches."""
+
+    def __init__(self, cfg, n_layers, max_tokens=1, eps=1e-6):
+        self.lib = load_library()
+        self.cfg = Config(cfg.hidden, cfg.n_experts, cfg.top_k, cfg.expert_inter, cfg.shared_inter, 64, max_tokens)
+        h = ctypes.c_void_p()
+        _check(self.lib.moe_stack_create(ctypes.byref(self.cfg), int(n_layers), float(eps), ctypes.byref(h)),
+               "moe_stack_create")
+        self.h = h
+        self.n_layers = n_layers
+        self.hidden = cfg.hidden
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.moe_stack_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def load_layer(self, layer, w: dict, stream=None):
+        W, keep, on_dev = _weights_struct(w)
+        _check(self.lib.moe_stack_load_layer(self.h, int(layer), ctypes.byref(W), int(on_dev), _stream_ptr(stream)),
+               "moe_stack_load_layer")
+
+    def forward(self, h_in, h_out=None, per_layer_out=None, stream=None):
+        """h_in: fp16 CUDA [T, H]; per_layer_out: None or fp16 CUDA [n_layers, T, H] (receives every h_{l+1})."""
+        import torch
+        assert h_in.dtype == torch.float16 and h_in.is_cuda and h_in.is_contiguous()
+        if h_out is None:
+            h_out = torch.empty_like(h_in)
+        if per_layer_out is not None:
+            assert per_layer_out.dtype == torch.float16 and per_layer_out.is_contiguous()
+            assert tuple(per_layer_out.shape) == (self.n_layers, *h_in.shape)
+        _check(self.lib.moe_stack_forward(self.h, _ptr(h_in), _ptr(h_out), h_in.shape[0], _ptr(per_layer_out),
+                                          _stream_ptr(stream)), "moe_stack_forward")
+        return h_out
+
+    def status(self):
+        f = ctypes.c_uint32(0)
+        s = self.lib.moe_stack_get_status(self.h, ctypes.byref(f))
+        return s, f.value
+
+    def layer_routing(self, layer, T):
+        """The routing record of one layer's last call (the block test hook on the stack's own handle)."""
+        import torch
+        K = self.cfg.top_k
+        hb = self.lib.moe_stack_layer(self.h, int(layer))
+        ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        _check(self.lib.moe_block_debug_last_routing(ctypes.c_void_p(hb), T, None, _ptr(ids), _ptr(w), None,
+                                                     _stream_ptr(None)), "moe_block_debug_last_routing")
+        return {"ids": ids, "w": w}
 
 
 def upload_weights(w: dict, device="cuda"):
