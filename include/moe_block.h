@@ -161,9 +161,11 @@ MOE_API int moe_block_debug_last_routing(moe_block_t *blk, int T, float *logits,
                                  float *sgate, void *stream);
 
 /* Test control of the bounded device waits: timeout_us = microseconds any device-side wait may last before
- * it gives up (0 = the default, 500 ms); skip_arrive = 1 makes CTA 0 withhold its logits arrival in the next
- * forward call only, so every CTA's bounded wait for the logits runs out and the call ends early with an
- * error bit set (the host then sees MOE_ERR_DEVICE_TIMEOUT from moe_block_get_status). */
+ * it gives up (0 = the default, 500 ms); skip_arrive = 1 withholds one arrival in the next forward call only:
+ * in the decode kernels the logits count of the CTA holding router row 0 (single token) or of CTA 0 (more
+ * tokens), so every CTA's bounded wait for the logits runs out; on the prompt-chunk path CTA 0's first weight
+ * copy of the router GEMM, so that CTA's waits for it run out. The call ends early with an error bit set and
+ * wrong outputs, and the host sees MOE_ERR_DEVICE_TIMEOUT from moe_block_get_status. No fault is involved. */
 MOE_API int moe_block_debug_set_wait(moe_block_t *blk, uint32_t timeout_us, int skip_arrive);
 
 /* Phase timestamps for performance analysis: when trace_device is non-NULL, every later decode call writes

@@ -302,7 +302,8 @@ static int run_forward(moe_block* b, const uint16_t* x, uint16_t* out, int T, co
     int n = 0;
     cudaError_t e = chunk_forward(b->L, b->G, b->CS, b->maps, b->cfg.max_tokens, b->num_sms, x, out, T, gamma, eps,
                                   b->rec_ids, b->rec_w,
-                                  b->rec_sg, b->status, b->timeout_ns, b->trace, st, &n);
+                                  b->rec_sg, b->status, b->timeout_ns, b->trace, st, &n, b->skip_arrive);
+    b->skip_arrive = 0;
     b->last_launches = n;
     if (e != cudaSuccess) return cuda_fail(e, "chunk forward");
     return MOE_OK;

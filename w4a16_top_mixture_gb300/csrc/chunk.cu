@@ -380,15 +380,16 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
                           int Tm, int num_sms,
                           const uint16_t* x, uint16_t* out, int T, const uint16_t* gamma, float eps,
                           int32_t* rec_ids, float* rec_w, float* rec_sg, uint32_t* status, uint64_t timeout_ns,
-                          uint64_t* trace, cudaStream_t st, int* launches) {
+                          uint64_t* trace, cudaStream_t st, int* launches, int skip) {
   const int E = L.E, K = L.K, H = L.H, TW = (T + 31) / 32;
   int n = 0;
   cudaError_t e = cudaMemsetAsync(S.masks, 0, (size_t)E * TW * 4, st);
   if (e != cudaSuccess) return e;
   k_chunk_prologue<<<(T + 7) / 8, 256, 0, st>>>(x, gamma, eps, T, H, S.xp);
   ++n;
-  GemmArgs ga{G, S, T, Tm, 1, status, timeout_ns, nullptr, maps};
+  GemmArgs ga{G, S, T, Tm, 1, status, timeout_ns, nullptr, maps, skip};
   e = chunk_gemm_launch(ga, num_sms, st);
+  ga.skip = 0;
   if (e != cudaSuccess) return e;
   ++n;
   k_chunk_route<<<(T + 7) / 8, 256, 0, st>>>(S.logits, E, K, T, S.ids, S.w, S.sg, S.masks, TW, rec_ids, rec_w,

@@ -89,6 +89,7 @@ struct GemmArgs {
   uint64_t timeout_ns;
   uint64_t* trace;   // optional: CTA 0's SM-clock stamps of its first 64 K-tiles, [role event][64]
   ChunkMaps maps;
+  int skip;          // test hook: CTA 0 withholds its first K-tile's copies, so its bounded waits run out
 };
 cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st);
 
@@ -97,6 +98,6 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
                           int Tm, int num_sms,
                           const uint16_t* x, uint16_t* out, int T, const uint16_t* gamma, float eps,
                           int32_t* rec_ids, float* rec_w, float* rec_sg, uint32_t* status, uint64_t timeout_ns,
-                          uint64_t* trace, cudaStream_t st, int* launches);
+                          uint64_t* trace, cudaStream_t st, int* launches, int skip = 0);
 
 }  // namespace moe

@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     if (lane == 0) {
       uint32_t gk = 0;
       bool run = true;
+      // test hook: CTA 0 never arms or fills the stage of its first K-tile, so the roles waiting for it time
+      // out and the CTA aborts
+      const bool withhold = g.skip && blockIdx.x == 0;
       JobIter it;
       job_begin(g, it);
       Job jb;
@@ -249,6 +252,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         for (int kt = 0; kt < jb.ktiles; ++kt, ++gk) {
           const int s = gk % NSG;
           if (gk >= NSG && !wait(&bar->empty[s], ((gk / NSG) & 1u) ^ 1u)) { run = false; break; }
+          if (withhold && gk == 0) continue;
           uint8_t* st = smem + s * ST_BYTES;
           mbar_expect_tx(&bar->full[s], (uint32_t)blk + bbytes * (jb.lomap >= 0 ? 2u : 1u));
           bulk_g2s(st + ST_W, jb.w + (size_t)kt * blk, (uint32_t)blk, &bar->full[s]);
@@ -257,9 +261,10 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
           GSTAMP(0, gk);
         }
       }
-      // drain: every copy issued must have landed before the CTA leaves
+      // drain: every copy issued must have landed before the CTA leaves (the withheld one was never issued)
       const uint32_t cnt = gk < (uint32_t)NSG ? gk : (uint32_t)NSG;
-      for (uint32_t q = gk - cnt; q < gk; ++q) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
+      for (uint32_t q = gk - cnt; q < gk; ++q)
+        if (!(withhold && q == 0)) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 14) {
