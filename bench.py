@@ -71,7 +71,7 @@ def peaks():
 
 def traffic_record():
     """DRAM bytes per launch from a committed ncu summary, valid only if the kernel source is unchanged."""
-    rec = os.path.join(ROOT, "profiles", "k_decode_prod_t1.json")
+    rec = os.path.join(ROOT, "profiles", "k_decode1_prod_t1.json")
     if not os.path.exists(rec):
         return None
     d = json.load(open(rec))

@@ -89,8 +89,15 @@ MOE_API int moe_block_load_weights(moe_block_t *blk, const moe_block_weights_t *
 
 /* out[T][H] = block(x[T][H]). x and out are caller-owned device buffers of fp16, 16-byte aligned, not
  * aliasing. 0 <= T <= max_tokens (T = 0 is a no-op). Asynchronous on `stream`, no host synchronisation and no
- * allocation, so it can be captured in a CUDA graph. T <= 16 runs the fused decode kernel; larger T the
- * prompt-chunk path. */
+ * allocation, so it can be captured in a CUDA graph. T <= 16 runs a fused decode kernel; larger T the
+ * prompt-chunk path.
+ *
+ * Residency. The decode kernels (one launch of one CTA per SM) hand results between their CTAs through
+ * grid-wide counts, so all CTAs of a launch must be resident at once; moe_block_create checks that the grid
+ * fits the device. A kernel of another stream, process or client that holds SMs while a forward runs can keep
+ * some of its CTAs from starting: the others then wait, bounded (500 ms by default), and the call ends without
+ * its result, which moe_block_get_status (and moe_block_forward_host, which reads the status itself) reports
+ * as MOE_ERR_DEVICE_TIMEOUT. Run forward with the SMs to itself, or poll the status. */
 MOE_API int moe_block_forward(moe_block_t *blk, const void *x, void *out, int T, void *stream);
 
 /* Same computation with HOST buffers: copies x to the device, runs forward and copies out back, then
@@ -179,9 +186,10 @@ MOE_API int moe_block_debug_set_wait(moe_block_t *blk, uint32_t timeout_us, int 
 MOE_API int moe_block_debug_set_trace(moe_block_t *blk, void *trace_device);
 
 /* ---- allocation-free routing ----
- * No counterpart on the pages: a convenience for callers that may not allocate device memory when they call
- * (inside CUDA stream capture, where cudaMalloc is illegal, or under a runtime whose allocator must own every
- * device byte). Computes the routing step of the block -- router logits from the CANONICAL int8 router
+ * No counterpart on the pages. For callers that cannot allocate device memory at the point of the call: a
+ * serving runtime whose own pool allocator must account for every device byte (memory taken with cudaMalloc
+ * behind its back breaks its budget), or a latency-critical decode loop that cannot afford cudaMalloc's
+ * implicit device-wide synchronisation. Computes the routing step of the block -- router logits from the CANONICAL int8 router
  * (router_q [E+1][H], router_s/b [E+1][H/64] fp16 bits, device memory), softmax over the E expert logits,
  * top-k, renormalisation, sigmoid of the shared-gate logit -- for x [T][H] fp16 (device) into ids [T][k] int32
  * (ascending), weights [T][k] fp32 and sgate [T] fp32 (device). It allocates nothing: the logits live in a

@@ -1,8 +1,9 @@
 """The allocation-free routing entry point (moe_router_topk_noalloc) against the regular forward's routing.
 
-It serves callers that may not allocate device memory when they call (inside CUDA stream capture, or under a
-runtime that owns every device byte): its scratch is a fixed array inside the library. This file is collected
-last so that a failure here cannot hide any other test."""
+It serves callers that cannot allocate device memory when they call (a serving runtime whose pool allocator
+must account for every device byte, a latency-critical loop that cannot afford cudaMalloc's device-wide
+synchronisation): its scratch is a fixed array inside the library. This file is collected last so that a failure
+here cannot hide any other test."""
 import ctypes
 
 import numpy as np

@@ -155,6 +155,27 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
     if (!decode_plan(b->L, T, b->num_sms, b->max_smem, &b->plans[T])) { delete b; return MOE_ERR_UNSUPPORTED; }
   }
   b->has_dec1 = decode1_plan(b->L, b->num_sms, b->max_smem, &b->plan1);
+  // the grid-wide counts of the decode kernels need every CTA of a launch resident at once: refuse a device
+  // on which the grid does not fit
+  {
+    int per_sm = 0;
+    if (b->has_dec1) {
+      if (decode1_occupancy(b->L, b->plan1, &per_sm) != cudaSuccess || per_sm * b->num_sms < b->plan1.grid)
+        b->has_dec1 = false;
+    }
+    for (int T = 1; T <= b->dec_T; ++T) {
+      per_sm = 0;
+      const cudaError_t oe = decode_occupancy(b->L, b->plans[T], &per_sm);
+      if (oe != cudaSuccess || per_sm * b->num_sms < b->plans[T].grid) {
+        const int grid = b->plans[T].grid;
+        delete b;
+        if (oe != cudaSuccess) return cuda_fail(oe, "decode occupancy");
+        snprintf(g_cuda_err, sizeof(g_cuda_err), "the decode grid of %d CTAs does not fit the device at once",
+                 grid);
+        return MOE_ERR_UNSUPPORTED;
+      }
+    }
+  }
   const MoeLayout& L = b->L;
   size_t total = L.router_bytes + L.shgu_bytes + L.shdn_bytes + L.exgu_bytes + L.exdn_bytes;
   cudaError_t e = cudaMalloc(&b->wstore, total);

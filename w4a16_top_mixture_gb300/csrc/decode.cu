@@ -753,25 +753,31 @@ bool decode_plan(const MoeLayout& L, int T, int grid, int max_smem, DecodeLaunch
 
 std::mutex g_dec_attr_mutex;
 
+// raise the dynamic shared-memory limit once per device and instantiation (the setting is per function and
+// per device)
 template <class SH, int TK>
-static cudaError_t launch_s(const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st) {
+static cudaError_t prepare_s(const DecodeLaunch& pl) {
   auto kern = k_decode<SH, TK>;
-  // raise the dynamic shared-memory limit once per device and instantiation (the setting is per function and
-  // per device)
   static int configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lk(g_dec_attr_mutex);
-    if (configured[dev] < pl.smem) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-      if (e != cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
-      if (e != cudaSuccess) return e;
-      configured[dev] = pl.smem > 232448 ? pl.smem : 232448;
-    }
+  std::lock_guard<std::mutex> lk(g_dec_attr_mutex);
+  if (configured[dev] < pl.smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = pl.smem > 232448 ? pl.smem : 232448;
   }
+  return cudaSuccess;
+}
+
+template <class SH, int TK>
+static cudaError_t launch_s(const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st) {
+  auto kern = k_decode<SH, TK>;
+  cudaError_t e = prepare_s<SH, TK>(pl);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(DEC_THREADS);
@@ -795,6 +801,19 @@ static bool is_shape(const MoeLayout& L) {
 }
 
 bool decode_supported(const MoeLayout& L) { return is_shape<ShapeProd>(L) || is_shape<ShapeTiny>(L); }
+
+template <class SH>
+static cudaError_t occupancy_s(const DecodeLaunch& pl, int* per_sm) {
+  cudaError_t e = prepare_s<SH, 2>(pl);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, k_decode<SH, 2>, DEC_THREADS, pl.smem);
+}
+
+cudaError_t decode_occupancy(const MoeLayout& L, const DecodeLaunch& pl, int* ctas_per_sm) {
+  if (is_shape<ShapeProd>(L)) return occupancy_s<ShapeProd>(pl, ctas_per_sm);
+  if (is_shape<ShapeTiny>(L)) return occupancy_s<ShapeTiny>(pl, ctas_per_sm);
+  return cudaErrorNotSupported;
+}
 
 cudaError_t decode_launch(const MoeLayout& L, const DecodeArgs& a, const DecodeLaunch& pl, cudaStream_t st) {
   if (is_shape<ShapeProd>(L)) return launch_s<ShapeProd, 2>(a, pl, st);

@@ -63,4 +63,9 @@ size_t decode_hbuf_floats(const MoeLayout& L, int T);
 bool decode1_plan(const MoeLayout& L, int grid, int max_smem, Decode1Launch* out);
 cudaError_t decode1_launch(const MoeLayout& L, const DecodeArgs& a, const Decode1Launch& pl, cudaStream_t st);
 
+// Host, on the current device: give the kernel of a plan its shared-memory limits and report how many of its
+// CTAs one SM holds at once (the grid-wide counts of both decode kernels need the whole grid resident).
+cudaError_t decode1_occupancy(const MoeLayout& L, const Decode1Launch& pl, int* ctas_per_sm);
+cudaError_t decode_occupancy(const MoeLayout& L, const DecodeLaunch& pl, int* ctas_per_sm);
+
 }  // namespace moe

@@ -589,25 +589,40 @@ static bool is_shape1(const MoeLayout& L) {
 std::mutex g_attr_mutex;
 int g_attr_smem[4][64];
 
+// the kernel's shared-memory attributes on the current device (once per device and instantiation)
 template <class SH, int KID>
-static cudaError_t launch1(const DecodeArgs& a, const Decode1Launch& pl, cudaStream_t st) {
-  const bool tr = a.trace != nullptr;
+static cudaError_t prepare1(bool tr, const Decode1Launch& pl) {
   auto kern = tr ? k_decode1<SH, true> : k_decode1<SH, false>;
   const int kid = KID * 2 + (tr ? 1 : 0);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lk(g_attr_mutex);
-    if (g_attr_smem[kid][dev] < pl.smem) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
-      // the whole unified L1/shared array as shared memory, so that two CTAs fit on one SM
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-      if (e != cudaSuccess) return e;
-      g_attr_smem[kid][dev] = pl.smem;
-    }
+  std::lock_guard<std::mutex> lk(g_attr_mutex);
+  if (g_attr_smem[kid][dev] < pl.smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    // the whole unified L1/shared array as shared memory, so that two CTAs fit on one SM
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    g_attr_smem[kid][dev] = pl.smem;
   }
+  return cudaSuccess;
+}
+
+template <class SH, int KID>
+static cudaError_t occupancy1(const Decode1Launch& pl, int* per_sm) {
+  cudaError_t e = prepare1<SH, KID>(false, pl);
+  if (e == cudaSuccess) e = prepare1<SH, KID>(true, pl);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, k_decode1<SH, false>, DEC1_THREADS, pl.smem);
+}
+
+template <class SH, int KID>
+static cudaError_t launch1(const DecodeArgs& a, const Decode1Launch& pl, cudaStream_t st) {
+  const bool tr = a.trace != nullptr;
+  auto kern = tr ? k_decode1<SH, true> : k_decode1<SH, false>;
+  cudaError_t e = prepare1<SH, KID>(tr, pl);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(DEC1_THREADS);
@@ -645,6 +660,12 @@ bool decode1_plan(const MoeLayout& L, int grid, int max_smem, Decode1Launch* out
   if (is_shape1<ShapeProd>(L)) return plan1_s<ShapeProd>(L, grid, max_smem, out);
   if (is_shape1<ShapeTiny>(L)) return plan1_s<ShapeTiny>(L, grid, max_smem, out);
   return false;
+}
+
+cudaError_t decode1_occupancy(const MoeLayout& L, const Decode1Launch& pl, int* ctas_per_sm) {
+  if (is_shape1<ShapeProd>(L)) return occupancy1<ShapeProd, 0>(pl, ctas_per_sm);
+  if (is_shape1<ShapeTiny>(L)) return occupancy1<ShapeTiny, 1>(pl, ctas_per_sm);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t decode1_launch(const MoeLayout& L, const DecodeArgs& a, const Decode1Launch& pl, cudaStream_t st) {

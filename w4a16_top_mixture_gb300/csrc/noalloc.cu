@@ -1,8 +1,8 @@
 // Allocation-free routing entry point (moe_router_topk_noalloc): the router GEMV and the softmax -> top-k ->
 // renormalise step of the block, reading the router in the canonical layout, with its logits scratch in a
-// fixed file-scope device array instead of memory from cudaMalloc. For callers that may not allocate device
-// memory at the point of the call: code running inside CUDA stream capture (cudaMalloc is illegal in global
-// capture mode), or runtimes whose device memory is owned by another allocator that must see every byte.
+// fixed file-scope device array instead of memory from cudaMalloc. For callers that cannot allocate device
+// memory at the point of the call: serving runtimes whose own pool allocator must account for every device
+// byte, and latency-critical loops that cannot afford cudaMalloc's implicit device-wide synchronisation.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <mutex>
