@@ -100,3 +100,54 @@ def test_all_zero_weights_give_exact_zero(cfgname, T):
     assert (wts == np.float32(1.0 / cfg.top_k)).all()
     assert (sg == 0.5).all()
     assert (out.view(np.uint16) == 0).all(), "output not exactly +0"
+
+
+def _valid_routing(ids, E, K):
+    assert ids.shape[1] == K
+    assert ((ids >= 0) & (ids < E)).all(), ids
+    assert (np.diff(ids, axis=1) > 0).all(), ids            # distinct and ascending
+
+
+@pytest.mark.parametrize("cfgname,T", CASES)
+def test_nonfinite_activations_keep_routing_in_bounds(cfgname, T):
+    """A token whose activations hold NaN or an infinity makes every router logit NaN (or infinite). The top k
+    must still name k distinct experts below E (everything downstream indexes by them), and the other tokens
+    of the call must come out as if that token were absent."""
+    import ctypes
+    import torch
+    cfg = synth.TINY if cfgname == "tiny" else synth.PROD
+    w = synth.gen_layer(cfg, 24)
+    x = synth.gen_x(cfg, T, 25)
+    bad = {0: np.float16(np.nan), 1: np.float16(np.inf), 2: np.float16(-np.inf)}
+    for t, v in bad.items():
+        if t < T and (T == 1 or t != T - 1):                 # the last token of a multi-token call stays finite
+            x[t, 5 * t + 3] = v
+    nonfinite = ~np.isfinite(x.astype(np.float32)).all(axis=1)
+    assert nonfinite.any() and (T == 1 or not nonfinite.all())
+    out, ids, wts, sg = _run(cfg, w, x, max_tokens=max(T, 16))
+    _valid_routing(ids, cfg.n_experts, cfg.top_k)
+    good = np.flatnonzero(~nonfinite)
+    if good.size:
+        r = O.block_forward(w, x[good], cfg.top_k)
+        np.testing.assert_array_equal(ids[good], r["ids"])
+        ok, e, plain = check_tol(out[good].astype(np.float64), r["out"])
+        assert ok, (e, plain)
+    # the allocation-free routing entry point, on the same tokens
+    L = lib.load_library()
+    dev = {n: torch.from_numpy(np.ascontiguousarray(w[n]).view(np.uint8)).cuda() for n in
+           ("router_q", "router_s", "router_b")}
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda()
+    ids2 = torch.empty((T, cfg.top_k), dtype=torch.int32, device="cuda")
+    w2 = torch.empty((T, cfg.top_k), dtype=torch.float32, device="cuda")
+    sg2 = torch.empty((T,), dtype=torch.float32, device="cuda")
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    s = L.moe_router_topk_noalloc(*(ctypes.c_void_p(dev[n].data_ptr()) for n in ("router_q", "router_s", "router_b")),
+                                  cfg.hidden, cfg.n_experts, cfg.top_k, ctypes.c_void_p(xd.data_ptr()), T,
+                                  ctypes.c_void_p(ids2.data_ptr()), ctypes.c_void_p(w2.data_ptr()),
+                                  ctypes.c_void_p(sg2.data_ptr()), st)
+    assert s == 0, s
+    torch.cuda.synchronize()
+    ids2 = ids2.cpu().numpy()
+    _valid_routing(ids2, cfg.n_experts, cfg.top_k)
+    if good.size:
+        np.testing.assert_array_equal(ids2[good], r["ids"])

@@ -6,6 +6,7 @@
 
 #include "chunk.cuh"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -112,6 +113,9 @@ size_t chunk_scratch_bytes(const MoeLayout& L, int Tm) {
   b += al256(TK * H * 2);
   b += al256(TK * I * 2) * 2 + al256(TK * H * 4);
   b += al256((E + TK / CHUNK_NT + 2) * 16) + al256(16 * 4);
+  const size_t sp = (T + 3) & ~(size_t)3, sr = (TK + 3) & ~(size_t)3;
+  b += al256(((H / 64) * sp + SUM_SLACK) * 4) + al256(((H / 64) * sr + SUM_SLACK) * 4);
+  b += al256(((Is / 64) * sp + SUM_SLACK) * 4) + al256(((I / 64) * sr + SUM_SLACK) * 4);
   return b;
 }
 
@@ -138,6 +142,13 @@ ChunkScratch chunk_scratch_carve(const MoeLayout& L, int Tm, uint8_t* base) {
   S.y = (float*)take(TK * H * 4);
   S.groups = (int4*)take((E + TK / CHUNK_NT + 2) * 16);
   S.ctl = (int32_t*)take(16 * 4);
+  const size_t sp = (T + 3) & ~(size_t)3, sr = (TK + 3) & ~(size_t)3;
+  S.sp = (int)sp;
+  S.sr = (int)sr;
+  S.sum_xp = (float*)take(((H / 64) * sp + SUM_SLACK) * 4);
+  S.sum_xs = (float*)take(((H / 64) * sr + SUM_SLACK) * 4);
+  S.sum_hs = (float*)take(((Is / 64) * sp + SUM_SLACK) * 4);
+  S.sum_hh = (float*)take(((I / 64) * sr + SUM_SLACK) * 4);
   return S;
 }
 
@@ -157,9 +168,9 @@ cudaError_t chunk_make_maps(const MoeLayout& L, const ChunkScratch& S, int Tm, C
   struct Buf { const uint16_t* p; int rows, cols; };
   const Buf bufs[CM_COUNT] = {{S.xp, Tm, L.H},  {S.xs, TK, L.H},    {S.hs, Tm, L.Is},
                               {S.hs_lo, Tm, L.Is}, {S.hh, TK, L.I}, {S.hh_lo, TK, L.I}};
-  const cuuint32_t boxrows[2] = {16, CHUNK_NT};
+  const cuuint32_t boxrows[CM_BOXES] = {16, 32, CHUNK_NT};
   for (int b = 0; b < CM_COUNT; ++b)
-    for (int v = 0; v < 2; ++v) {
+    for (int v = 0; v < CM_BOXES; ++v) {
       const cuuint64_t dims[2] = {(cuuint64_t)bufs[b].cols, (cuuint64_t)bufs[b].rows};
       const cuuint64_t strides[1] = {(cuuint64_t)bufs[b].cols * 2};
       const cuuint32_t box[2] = {64, boxrows[v]};
@@ -181,9 +192,10 @@ __device__ __forceinline__ float warp_sum_c(float v) {
   return v;
 }
 
-// x (or RMSNorm(h) * gamma rounded to fp16) -> xp in P8 order; one warp per token
+// x (or RMSNorm(h) * gamma rounded to fp16) -> xp in P8 order, and the sum of each 64-column group of the
+// written values -> sum_xp[g][t]; one warp per token
 __global__ void k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
-                                 int T, int H, uint16_t* __restrict__ xp) {
+                                 int T, int H, uint16_t* __restrict__ xp, float* __restrict__ sum_xp, int sp) {
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (t >= T) return;
   const uint16_t* xr = x + (size_t)t * H;
@@ -197,9 +209,11 @@ __global__ void k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t*
     ss = warp_sum_c(ss);
     rn = 1.0f / sqrtf(ss / (float)H + eps);
   }
+  // H / 8 is a multiple of 8, so the 8 blocks of a group sit on 8 neighbouring lanes of one iteration
   for (int blk = lane; blk < H / 8; blk += 32) {
     {
       uint16_t o[8];
+      float part = 0.f;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int c = blk * 8 + k;
@@ -208,7 +222,12 @@ __global__ void k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t*
           v = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(v)) * rn *
                                                __half2float(__ushort_as_half(gamma[c]))));
         o[p8pos(k)] = v;
+        part += __half2float(__ushort_as_half(v));
       }
+      part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
+      part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
+      part += __shfl_xor_sync(0xFFFFFFFFu, part, 4);
+      if ((blk & 7) == 0) sum_xp[(size_t)(blk >> 3) * sp + t] = part;
       uint4 pk;
       pk.x = o[0] | ((uint32_t)o[1] << 16);
       pk.y = o[2] | ((uint32_t)o[3] << 16);
@@ -220,44 +239,19 @@ __global__ void k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t*
 }
 
 // softmax over the E expert logits -> the k largest (lower index on ties) -> renormalise; sigmoid of logit E.
-// One warp per token; ids ascending. Also marks the token in its experts' masks.
+// One warp per token; ids ascending. Also marks the token in its experts' masks. EPL: logits per lane,
+// 32 * EPL >= E. The ids are below E whatever the logits hold (NaN and infinities included), so the masks and
+// everything indexed by an id stay in bounds.
+template <int EPL>
 __global__ void k_chunk_route(const float* __restrict__ logits, int E, int K, int T, int32_t* __restrict__ ids,
                               float* __restrict__ w, float* __restrict__ sg, uint32_t* __restrict__ masks, int TW,
                               int32_t* rec_ids, float* rec_w, float* rec_sg) {
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* lg = logits + (size_t)t * (E + 1);
-  constexpr int MAXEPL = 16;
-  const int epl = (E + 31) / 32;
-  float v[MAXEPL];
-#pragma unroll
-  for (int i = 0; i < MAXEPL; ++i) {
-    const int e = lane * epl + i;
-    v[i] = (i < epl && e < E) ? lg[e] : -INFINITY;
-  }
-  int sel_idx = -1;
-  float sel_val = 0.f;
-  for (int j = 0; j < K; ++j) {
-    float best = -INFINITY;
-    int bi = 0;
-#pragma unroll
-    for (int i = 0; i < MAXEPL; ++i)
-      if (v[i] > best) { best = v[i]; bi = i; }
-    int be = best == -INFINITY ? 0x7FFFFFFF : lane * epl + bi;
-    float m = best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-      if (om > m || (om == m && oe < be)) { m = om; be = oe; }
-    }
-    if (be == lane * epl + bi && best == m) {
-#pragma unroll
-      for (int i = 0; i < MAXEPL; ++i)
-        if (i == bi) v[i] = -INFINITY;
-    }
-    if (lane == j) { sel_idx = be; sel_val = m; }
-  }
+  int sel_idx;
+  float sel_val;
+  warp_topk_lean<EPL, false>(lg, E, K, sel_idx, sel_val);
   const float mx = __shfl_sync(0xFFFFFFFFu, sel_val, 0);
   const float ex = lane < K ? __expf(sel_val - mx) : 0.f;
   const float z = warp_sum_c(ex);
@@ -279,9 +273,9 @@ __global__ void k_chunk_route(const float* __restrict__ logits, int E, int K, in
 
 // One CTA of BUCKET_THREADS: per-expert token counts from the masks, exclusive scan, the sorted row of every
 // (token, slot), the token of every sorted row, and the list of row tiles (expert, first row, rows <= CHUNK_NT);
-// ctl[0] = tile count. Tokens of an expert keep their order. With a prefix table (dynamic shared memory of
-// E * TW ints: the tokens of expert e in mask words before word q), a pair's rank is one table read and one
-// mask word; without it (very long chunks) the rank counts the earlier words.
+// ctl[0] = tile count, ctl[1] = rows of the widest tile. Tokens of an expert keep their order. With a prefix
+// table (dynamic shared memory of E * TW ints: the tokens of expert e in mask words before word q), a pair's
+// rank is one table read and one mask word; without it (very long chunks) the rank counts the earlier words.
 constexpr int BUCKET_THREADS = 1024;
 constexpr size_t BUCKET_TABLE_MAX = 40960;   // prefix-table bytes that fit beside the static arrays in 48 KB
 __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t* __restrict__ masks, int E, int TW,
@@ -291,7 +285,7 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
                                                                  int4* __restrict__ groups,
                                                                  int32_t* __restrict__ ctl, int use_table) {
   extern __shared__ int pre[];   // [E][TW] when use_table
-  __shared__ int cnt[512], off[512], goff[512], wsum[32], wgsum[32];
+  __shared__ int cnt[512], off[512], goff[512], wsum[32], wgsum[32], wmax[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
   // counts (thread = expert) and the prefix table
   int c = 0;
@@ -329,7 +323,14 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
     goff[tid] = (warp > 0 ? wgsum[warp - 1] : 0) + gv - ng;
   }
   if (tid == 0) ctl[0] = wgsum[NW - 1];
+  // rows of the widest row tile
+  int wide = __reduce_max_sync(0xFFFFFFFFu, min(c, CHUNK_NT));
+  if (lane == 0) wmax[warp] = wide;
   __syncthreads();
+  if (warp == 0) {
+    wide = __reduce_max_sync(0xFFFFFFFFu, lane < NW ? wmax[lane] : 0);
+    if (lane == 0) ctl[1] = wide;
+  }
   for (int e = tid; e < E; e += blockDim.x)
     for (int g = 0; g * CHUNK_NT < cnt[e]; ++g)
       groups[goff[e] + g] = make_int4(e, off[e] + g * CHUNK_NT, min(CHUNK_NT, cnt[e] - g * CHUNK_NT), 0);
@@ -349,15 +350,17 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
   }
 }
 
-// xs[row] = xp[tok_of[row]] (fp16 rows of H); one warp per row
-__global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const int32_t* __restrict__ tok_of, int rows, int H,
-                               uint16_t* __restrict__ xs) {
+// xs[row] = xp[tok_of[row]] (fp16 rows of H) and its group sums; one warp per row
+__global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const float* __restrict__ sum_xp, int sp,
+                               const int32_t* __restrict__ tok_of, int rows, int H, uint16_t* __restrict__ xs,
+                               float* __restrict__ sum_xs, int sr) {
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (r >= rows) return;
   const int t = tok_of[r];
   const uint4* src = reinterpret_cast<const uint4*>(xp + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
   for (int i = lane; i < H / 8; i += 32) dst[i] = src[i];
+  for (int g = lane; g < H / 64; g += 32) sum_xs[(size_t)g * sr + r] = sum_xp[(size_t)g * sp + t];
 }
 
 // out[t][r] = sum_j w[t][j] * y[slot(t, j)][r] + sg[t] * ys[t][r] (+ h[t][r]), rounded to fp16 once
@@ -385,15 +388,18 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   int n = 0;
   cudaError_t e = cudaMemsetAsync(S.masks, 0, (size_t)E * TW * 4, st);
   if (e != cudaSuccess) return e;
-  k_chunk_prologue<<<(T + 7) / 8, 256, 0, st>>>(x, gamma, eps, T, H, S.xp);
+  k_chunk_prologue<<<(T + 7) / 8, 256, 0, st>>>(x, gamma, eps, T, H, S.xp, S.sum_xp, S.sp);
   ++n;
   GemmArgs ga{G, S, T, Tm, 1, status, timeout_ns, nullptr, maps, skip};
   e = chunk_gemm_launch(ga, num_sms, st);
   ga.skip = 0;
   if (e != cudaSuccess) return e;
   ++n;
-  k_chunk_route<<<(T + 7) / 8, 256, 0, st>>>(S.logits, E, K, T, S.ids, S.w, S.sg, S.masks, TW, rec_ids, rec_w,
-                                              rec_sg);
+  {
+    auto* route = E <= 32 ? k_chunk_route<1> : E <= 64 ? k_chunk_route<2> : E <= 128 ? k_chunk_route<4>
+                  : E <= 256 ? k_chunk_route<8> : k_chunk_route<16>;
+    route<<<(T + 7) / 8, 256, 0, st>>>(S.logits, E, K, T, S.ids, S.w, S.sg, S.masks, TW, rec_ids, rec_w, rec_sg);
+  }
   ++n;
   // the prefix table fits in shared memory for chunks up to tens of thousands of tokens
   const size_t tbl = (size_t)E * TW * sizeof(int);
@@ -401,7 +407,7 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   k_chunk_bucket<<<1, BUCKET_THREADS, use_table ? tbl : 0, st>>>(S.masks, E, TW, T, K, S.ids, S.slot_of, S.tok_of,
                                                                  S.groups, S.ctl, use_table);
   ++n;
-  k_chunk_gather<<<(T * K + 7) / 8, 256, 0, st>>>(S.xp, S.tok_of, T * K, H, S.xs);
+  k_chunk_gather<<<(T * K + 7) / 8, 256, 0, st>>>(S.xp, S.sum_xp, S.sp, S.tok_of, T * K, H, S.xs, S.sum_xs, S.sr);
   ++n;
   ga.phase = 2;
   ga.trace = trace;     // the trace holds the expert gate/up launch

@@ -19,7 +19,9 @@
 // The GEMM multiplies the exact integer codes (as fp16) by the activations on the tensor cores, one K-tile
 // (one group) at a time into a fresh accumulator, and folds each K-tile in fp32: acc += s * D + b * sum(x),
 // with sum(x) the activations' sum over the tile's 64 columns. Activation tiles arrive by TMA tensor loads
-// (128-byte swizzled, the layout the MMA reads) through tensor maps made once per handle.
+// (128-byte swizzled, the layout the MMA reads) through tensor maps made once per handle. The sums are made once
+// per activation row by the kernel that writes the row (the prologue, the gather, the SwiGLU epilogue) and kept
+// K-tile-major, sum[kt][row], so that one K-tile's sums for a tile of rows are one short contiguous run.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -47,7 +49,12 @@ cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, cudaStream_t st
 
 constexpr int CHUNK_NT = 64;   // tokens (rows of activations) per GEMM tile
 
-// scratch of the chunk path for up to Tm tokens. Activation sums are stored K-tile-major: sum[kt][row].
+// scratch of the chunk path for up to Tm tokens. Activation sums are stored K-tile-major, sum[kt][row], with a
+// row stride of sp (token order) or sr (expert-sorted order) floats, both multiples of 4, and SUM_SLACK floats
+// after the last K-tile's run: a K-tile's run for a tile of rows is fetched as SUM_RUN floats from its row
+// rounded down to a multiple of 4 (16-byte aligned bulk copies).
+constexpr int SUM_RUN = 68;
+constexpr int SUM_SLACK = 128;
 struct ChunkScratch {
   uint16_t* xp;        // [Tm][H] fp16, P8 order (block input, after RMSNorm in residual mode)
   float* logits;       // [Tm][E+1]
@@ -65,16 +72,22 @@ struct ChunkScratch {
   uint16_t* hh_lo;     // [Tm*K][I] fp16 P8, routed h (low half, scaled by 4096)
   float* y;            // [Tm*K][H] routed expert outputs (unweighted)
   int4* groups;        // [E + Tm*K/CHUNK_NT + 1] (expert, first sorted row, rows) per row tile
-  int32_t* ctl;        // [16] group count
+  int32_t* ctl;        // [16] ctl[0] row-tile count, ctl[1] rows of the widest row tile
+  float* sum_xp;       // [H/64][sp]   sums of xp's rows
+  float* sum_xs;       // [H/64][sr]   sums of xs's rows
+  float* sum_hs;       // [Is/64][sp]  sums of hs + hs_lo / 4096
+  float* sum_hh;       // [I/64][sr]   sums of hh + hh_lo / 4096
+  int sp, sr;          // row strides of the sums
 };
 size_t chunk_scratch_bytes(const MoeLayout& L, int Tm);
 ChunkScratch chunk_scratch_carve(const MoeLayout& L, int Tm, uint8_t* base);
 
-// TMA tensor maps of the GEMMs' activation operands: [buffer][box], boxes of 64 columns x 16 or 64 rows,
+// TMA tensor maps of the GEMMs' activation operands: [buffer][box], boxes of 64 columns x 16, 32 or 64 rows,
 // 128-byte swizzle, rows past the buffer read as zero
 enum : int { CM_XP = 0, CM_XS, CM_HS, CM_HSLO, CM_HH, CM_HHLO, CM_COUNT };
+constexpr int CM_BOXES = 3;
 struct ChunkMaps {
-  CUtensorMap m[CM_COUNT][2];
+  CUtensorMap m[CM_COUNT][CM_BOXES];
 };
 cudaError_t chunk_make_maps(const MoeLayout& L, const ChunkScratch& S, int Tm, ChunkMaps* out);
 

@@ -9,19 +9,19 @@
 //
 // Persistent CTAs (one per SM) take jobs j = blockIdx.x + k * gridDim.x. Warp roles, all stepping through the
 // same jobs and K-tiles and handing stages over on mbarriers:
-//   warp 0     producer (one lane): a bulk copy of the K-tile's weight block (codes + pairs) and TMA tensor
-//              loads of the activation rows (128-byte swizzled K-major), all on the stage's "full" barrier
+//   warps 0, 15  producers of the even (warp 0) or odd (warp 15) K-tiles: a bulk copy of the K-tile's weight
+//              block (codes + pairs), TMA tensor loads of the activation rows (128-byte swizzled K-major) and a
+//              bulk copy of the rows' sums over the K-tile's 64 columns, all on the stage's "full" barrier
 //   warps 1, 14  lane 0 issues the MMAs of the even (warp 1) or odd (warp 14) K-tiles (A from tensor memory,
 //              B from shared memory) and commits them to the stage's "empty" barrier; warp 1 also owns TMEM
 //   warps 2-9  dequantise, two groups of four warps taking alternate K-tiles: thread = band row = TMEM lane,
-//              codes -> exact fp16 integers stored straight into the slot's A columns of tensor memory; the
-//              group also sums the tile's activation rows (the fold's sum(x)), one (row, 16-byte chunk) item
-//              per thread
+//              codes -> exact fp16 integers stored straight into the slot's A columns of tensor memory
 //   warps 10-13 fold (thread = TMEM lane = band row) and, after the job's last K-tile, the epilogue
-// K-tile gk uses shared-memory stage gk % NSG and tensor-memory slot gk % nt (A operand, accumulator and side
-// buffer); there are more stages than slots so that more weight copies are in flight. Slots hold a low-half
-// accumulator only in phase 3 (the down projections, whose B is split into hi + lo halves), so phases 1 and 2
-// fit 5 slots into the 512 columns and phase 3 fits 3. Handoffs:
+// K-tile gk uses shared-memory stage gk % nsg and tensor-memory slot gk % nt (A operand, accumulator and side
+// buffer); there are more stages than slots so that more weight copies are in flight. A slot's accumulator is
+// as wide as the launch's widest job, and it has a low-half accumulator only in phase 3 (the down
+// projections, whose B is split into hi + lo halves): 8 slots fit the 512 columns when no job is wider than 32
+// rows, 5 (phase 3: 3) at 64. Handoffs:
 //   full[s]    the copies landed                                     (producer -> dequantisation)
 //   a_ready[t] A and the side buffer are written                     (dequantisation -> MMA)
 //   empty[s]   the dequantisation has read the stage and the MMAs have completed: the stage is free and the
@@ -44,21 +44,37 @@ namespace {
 
 enum : int { GK_ROUTER = 0, GK_SHGU = 1, GK_SHDN = 2, GK_EXGU = 3, GK_EXDN = 4 };
 
-constexpr int GTH = 480;                // 15 warps
-constexpr int NSG = 6;                  // shared-memory stages
-constexpr int NT_MAX = 5;               // tensor-memory slots (phases 1 and 2; phase 3: 3)
-// tensor-memory slot: accumulator hi (64 columns) | [phase 3: accumulator lo (64)] | A: 128 rows x 64 fp16
-// (32 columns)
-constexpr uint32_t TM_LO = 64;
-static_assert(5 * 96 <= 512 && 3 * 160 <= 512, "tensor memory");
-// stage layout: weight block | B hi (64 rows x 128 B, swizzled) | B lo
-constexpr int ST_W = 0, ST_BHI = 9216, ST_BLO = 17408, ST_BYTES = 25600;
-constexpr int S_SIDE = NSG * ST_BYTES;              // NT_MAX side buffers: (s, b) of 128 rows, 64 row sums
+constexpr int GTH = 512;                // 16 warps
+constexpr int NSG_MAX = 16;             // shared-memory stages (the count depends on the phase, see Geo)
+constexpr int NT_MAX = 8;               // tensor-memory slots (the count depends on the widest tile, see Slots)
+// The stages share one area. A stage is weight block | B hi (up to 64 rows x 128 B, swizzled) | [B lo], each
+// part 1024-byte aligned (the 128-byte swizzle's period). Its size depends on the phase, and so does the number
+// of stages: the fewer bytes a K-tile needs, the more K-tiles are in flight (the copies' latency is what the
+// pipeline has to cover).
+constexpr int ST_AREA = 186368;
+struct Geo {
+  int nsg, bytes, bhi, blo;
+};
+__host__ __device__ constexpr Geo geo_of(int phase) {
+  return phase == 1 ? Geo{10, 17408, 9216, 9216}       // int8 router / shared gate-up blocks, B hi
+         : phase == 2 ? Geo{14, 13312, 5120, 5120}     // int4 expert gate/up blocks, B hi
+                      : Geo{7, 25600, 9216, 17408};    // int4 / int8 down blocks, B hi and lo
+}
+static_assert(geo_of(1).nsg * geo_of(1).bytes <= ST_AREA && geo_of(2).nsg * geo_of(2).bytes <= ST_AREA &&
+                  geo_of(3).nsg * geo_of(3).bytes <= ST_AREA && geo_of(2).nsg <= NSG_MAX,
+              "stages");
+static_assert(GEMM_BLK8 <= 9216 && GEMM_BLK4 <= 5120, "weight block fits before B");
+constexpr int ST_W = 0;
+constexpr int S_SIDE = ST_AREA;                     // NT_MAX side buffers: (s, b) of 128 rows, 64 row sums
 constexpr int SIDE_BYTES = 128 * 4 + 64 * 4;
-constexpr int S_EP = S_SIDE + NT_MAX * SIDE_BYTES;  // epilogue staging of a job's accumulator: [128][65]
+constexpr int S_SUMS = S_SIDE + NT_MAX * SIDE_BYTES;  // per stage: the K-tile's run of activation sums
+constexpr int SUMS_BYTES = SUM_RUN * 4;
+static_assert(SUMS_BYTES % 16 == 0 && S_SUMS % 16 == 0, "bulk-copy alignment");
+constexpr int S_EP = S_SUMS + NSG_MAX * SUMS_BYTES;  // epilogue staging of a job's accumulator: [128][65]
 constexpr int S_BAR = S_EP + 128 * 65 * 4;
-constexpr int S_BYTES = S_BAR + 256;
+constexpr int S_BYTES = S_BAR + 512;
 constexpr int GEMM_SMEM = S_BYTES + 1024;           // + alignment slack
+static_assert(GEMM_SMEM <= 232448, "shared memory");
 constexpr uint32_t ERR_GEMM_WAIT = 512u;
 
 struct Job {
@@ -67,9 +83,12 @@ struct Job {
   int ktiles, int8;
   int bmap, lomap;        // tensor maps of the activations and of their low halves (-1: none)
   int row0, cnt, n;       // first activation row, rows, MMA N (cnt rounded up to 16)
+  const float* sum;       // K-tile-major sums of the activation rows
+  int sstride;            // their row stride
 };
 
-// tensor-memory slot of a role's current K-tile and the parity of that slot's current use
+// a ring position (tensor-memory slot or shared-memory stage) of a role's current K-tile and the parity of the
+// position's current use
 struct SlotRing {
   int t = 0;
   uint32_t ph = 0;
@@ -80,28 +99,30 @@ struct SlotRing {
 
 // Job j of the phase. Phases 2 and 3 take the expert row-tile count (ngroups) and job j's row-tile entry gr
 // (S.groups[j % ngroups] for the expert jobs) from the caller, which loads them ahead of time.
-__device__ __forceinline__ bool decode_job(const GemmArgs& g, int j, int ngroups, int4 gr, Job& jb) {
+// Token tiles (phase 1, and the shared down of phase 3) are tw rows wide.
+__device__ __forceinline__ bool decode_job(const GemmArgs& g, int j, int ngroups, int tw, int4 gr, Job& jb) {
   const GemmLayout& G = g.G;
+  const ChunkScratch& S = g.S;
   const int H = G.H, I = G.I, Is = G.Is, T = g.T;
-  const int NTT = (T + CHUNK_NT - 1) / CHUNK_NT;
+  const int NTT = (T + tw - 1) / tw;
   jb.e = 0;
   jb.lomap = -1;
   auto token_tile = [&](int nt) {
-    jb.row0 = nt * CHUNK_NT;
-    jb.cnt = min(CHUNK_NT, T - jb.row0);
+    jb.row0 = nt * tw;
+    jb.cnt = min(tw, T - jb.row0);
   };
   if (g.phase == 1) {
     const int MTr = G.Mr / 128, MTs = 2 * Is / 128;
     if (j < MTr * NTT) {
       jb.kind = GK_ROUTER; jb.m = j % MTr; token_tile(j / MTr);
       jb.w = G.gr + (size_t)jb.m * (H / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = H / 64;
-      jb.bmap = CM_XP;
+      jb.bmap = CM_XP; jb.sum = S.sum_xp; jb.sstride = S.sp;
     } else {
       j -= MTr * NTT;
       if (j >= MTs * NTT) return false;
       jb.kind = GK_SHGU; jb.m = j % MTs; token_tile(j / MTs);
       jb.w = G.gsgu + (size_t)jb.m * (H / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = H / 64;
-      jb.bmap = CM_XP;
+      jb.bmap = CM_XP; jb.sum = S.sum_xp; jb.sstride = S.sp;
     }
   } else {
     const int MTg = 2 * I / 128, MTd = H / 128;
@@ -114,18 +135,18 @@ __device__ __forceinline__ bool decode_job(const GemmArgs& g, int j, int ngroups
       if (g.phase == 2) {
         jb.kind = GK_EXGU;
         jb.w = G.gegu + (size_t)gr.x * G.gegu_expert + (size_t)m * (H / 64) * GEMM_BLK4; jb.ktiles = H / 64;
-        jb.bmap = CM_XS;
+        jb.bmap = CM_XS; jb.sum = S.sum_xs; jb.sstride = S.sr;
       } else {
         jb.kind = GK_EXDN;
         jb.w = G.gedn + (size_t)gr.x * G.gedn_expert + (size_t)m * (I / 64) * GEMM_BLK4; jb.ktiles = I / 64;
-        jb.bmap = CM_HH; jb.lomap = CM_HHLO;
+        jb.bmap = CM_HH; jb.lomap = CM_HHLO; jb.sum = S.sum_hh; jb.sstride = S.sr;
       }
     } else {
       j -= nex;
       if (g.phase != 3 || j >= MTd * NTT) return false;
       jb.kind = GK_SHDN; jb.m = j % MTd; token_tile(j / MTd);
       jb.w = G.gsdn + (size_t)jb.m * (Is / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = Is / 64;
-      jb.bmap = CM_HS; jb.lomap = CM_HSLO;
+      jb.bmap = CM_HS; jb.lomap = CM_HSLO; jb.sum = S.sum_hs; jb.sstride = S.sp;
     }
   }
   jb.n = (jb.cnt + 15) & ~15;
@@ -135,7 +156,7 @@ __device__ __forceinline__ bool decode_job(const GemmArgs& g, int j, int ngroups
 // A role's walk over its CTA's jobs j = blockIdx.x + k * gridDim.x. The row-tile entry of the next job is
 // loaded while the current one runs, so a job change costs no global-memory round trip.
 struct JobIter {
-  int j, ngroups;
+  int j, ngroups, tw;
   int4 gr;
 };
 __device__ __forceinline__ int4 job_group(const GemmArgs& g, int ngroups, int j) {
@@ -143,39 +164,33 @@ __device__ __forceinline__ int4 job_group(const GemmArgs& g, int ngroups, int j)
   if (g.phase == 1 || ngroups <= 0 || j >= MT * ngroups) return make_int4(0, 0, 0, 0);
   return g.S.groups[j % ngroups];
 }
-__device__ __forceinline__ void job_begin(const GemmArgs& g, JobIter& it) {
+__device__ __forceinline__ void job_begin(const GemmArgs& g, int ngroups, int tw, JobIter& it) {
   it.j = blockIdx.x;
-  it.ngroups = g.phase == 1 ? 0 : g.S.ctl[0];
+  it.ngroups = ngroups;
+  it.tw = tw;
   it.gr = job_group(g, it.ngroups, it.j);
 }
 __device__ __forceinline__ bool job_next(const GemmArgs& g, JobIter& it, Job& jb) {
-  const bool ok = decode_job(g, it.j, it.ngroups, it.gr, jb);
+  const bool ok = decode_job(g, it.j, it.ngroups, it.tw, it.gr, jb);
   it.j += gridDim.x;
   it.gr = job_group(g, it.ngroups, it.j);
   return ok;
 }
 
 struct Bars {
-  uint64_t full[NSG], empty[NSG], a_ready[NT_MAX], d_free[NT_MAX];
+  uint64_t full[NSG_MAX], empty[NSG_MAX], a_ready[NT_MAX], d_free[NT_MAX];
   uint64_t fold_sync;   // the four fold warps meet here in the SwiGLU epilogue (a bounded wait)
   uint32_t tslot;
+  int ngroups, tw;      // the launch's row-tile count and token-tile width, read once
   volatile int abort;
 };
+static_assert(sizeof(Bars) <= S_BYTES - S_BAR, "barrier area");
 
 // debug stamps (CTA 0, first 64 K-tiles): events 0 producer issued, 1 dequant saw the stage, 2 dequant done,
 // 3 MMA issued, 4 fold saw the accumulator, 5 fold done, 6 MMA saw A ready
 #define GSTAMP(ev, k) do { if (g.trace && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
 
 __device__ __forceinline__ float silu_c(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
-
-// sum of the 8 fp16 values of a 16-byte chunk, in fp32
-__device__ __forceinline__ float sum8_h(uint4 v) {
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-  const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
-  const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
-  return ((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y));
-}
 
 // position of unit u of an h vector in P8 order
 __device__ __forceinline__ int p8u(int u) {
@@ -201,7 +216,6 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     atomicOr(g.status, ERR_GEMM_WAIT);
     bar->abort = 1;
   };
-  // bounded wait on phase parity `ph` of `b`; false (and the CTA aborts) on a timeout or an earlier abort
   // bounded wait on phase parity `ph` of `b`; false (and the CTA aborts) on a timeout; a wait that does not
   // complete at once gives up straight away if the CTA has already aborted
   auto wait = [&](uint64_t* b, uint32_t ph) -> bool {
@@ -212,7 +226,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   };
 
   if (tid == 0) {
-    for (int s = 0; s < NSG; ++s) {
+    for (int s = 0; s < NSG_MAX; ++s) {
       mbar_init(&bar->full[s], 1);          // the producer's expect-tx arrival
       mbar_init(&bar->empty[s], 4 + 1);     // dequant warps (codes, pairs, sums read) + MMA commit (B read)
     }
@@ -222,6 +236,10 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     }
     mbar_init(&bar->fold_sync, 4);
     bar->abort = 0;
+    // phase 1 tiles the tokens 64 at a time; phases 2 and 3 take the bucketing's row tiles, and phase 3 tiles
+    // the shared down's tokens as wide as the widest row tile, so no job is wider than that
+    bar->ngroups = g.phase == 1 ? 0 : g.S.ctl[0];
+    bar->tw = g.phase == 1 ? CHUNK_NT : min(CHUNK_NT, max(16, (g.S.ctl[1] + 15) & ~15));
     fence_mbar_init();
   }
   if (warp == 1) { tmem_alloc(&bar->tslot, 512); tmem_relinquish(); }
@@ -229,42 +247,68 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar->tslot;
-  // slot geometry of this phase
+  const Geo geo = geo_of(g.phase);
+  const uint32_t NSG = (uint32_t)geo.nsg;
+  const int ngroups = bar->ngroups, tw = bar->tw;
+  // slot geometry: accumulator hi (aw columns) | [phase 3: accumulator lo (aw)] | A: 128 rows x 64 fp16 (32
+  // columns), aw = the widest job's N rounded up to 32 columns; as many slots as fit the 512 columns
   const bool lo_phase = g.phase == 3;
-  const int nt = lo_phase ? 3 : 5;
-  const uint32_t slot_cols = lo_phase ? 160u : 96u, a_col = lo_phase ? 128u : 64u;
+  const uint32_t aw = (uint32_t)((min(tw, g.phase == 1 ? ((min(g.T, CHUNK_NT) + 15) & ~15) : CHUNK_NT) + 31) & ~31);
+  const uint32_t tlo = aw, a_col = lo_phase ? 2 * aw : aw, slot_cols = a_col + 32;
+  const int nt = min(NT_MAX, (int)(512 / slot_cols));
+  float* sums = reinterpret_cast<float*>(smem + S_SUMS);   // [NSG_MAX][SUM_RUN]
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer (lane 0)
-    if (lane == 0) {
-      uint32_t gk = 0;
-      bool run = true;
-      // test hook: CTA 0 never arms or fills the stage of its first K-tile, so the roles waiting for it time
-      // out and the CTA aborts
-      const bool withhold = g.skip && blockIdx.x == 0;
-      JobIter it;
-      job_begin(g, it);
-      Job jb;
-      while (run && job_next(g, it, jb)) {
-        const int blk = jb.int8 ? GEMM_BLK8 : GEMM_BLK4;
-        const int box = jb.n <= 16 ? 0 : 1;
-        const uint32_t bbytes = (box ? CHUNK_NT : 16) * 128;
-        for (int kt = 0; kt < jb.ktiles; ++kt, ++gk) {
-          const int s = gk % NSG;
-          if (gk >= NSG && !wait(&bar->empty[s], ((gk / NSG) & 1u) ^ 1u)) { run = false; break; }
-          if (withhold && gk == 0) continue;
-          uint8_t* st = smem + s * ST_BYTES;
-          mbar_expect_tx(&bar->full[s], (uint32_t)blk + bbytes * (jb.lomap >= 0 ? 2u : 1u));
-          bulk_g2s(st + ST_W, jb.w + (size_t)kt * blk, (uint32_t)blk, &bar->full[s]);
-          tma_load_2d(st + ST_BHI, &g.maps.m[jb.bmap][box], kt * 64, jb.row0, &bar->full[s]);
-          if (jb.lomap >= 0) tma_load_2d(st + ST_BLO, &g.maps.m[jb.lomap][box], kt * 64, jb.row0, &bar->full[s]);
-          GSTAMP(0, gk);
-        }
+  if (warp == 0 || warp == 15) {
+    // ------------------------------------------------------------------ producers
+    // Warp 0 fills the stages of the even K-tiles, warp 15 those of the odd ones: issuing a copy costs its
+    // thread about a hundred cycles, too slow for one thread to keep up. The warp steps through the loop
+    // together; lane 0 arms the stage, and lanes 0 and 1 issue their copies in one instruction each: the
+    // weight block and the sums run (1-D bulk copies), then B hi and B lo (tensor loads).
+    const uint32_t par = warp == 0 ? 0u : 1u;
+    uint32_t gk = 0;
+    bool run = true;
+    // test hook: CTA 0 never arms or fills the stage of its first K-tile, so the roles waiting for it time
+    // out and the CTA aborts
+    const bool withhold = g.skip && blockIdx.x == 0;
+    JobIter it;
+    job_begin(g, ngroups, tw, it);
+    Job jb;
+    SlotRing sr;
+    while (run && job_next(g, it, jb)) {
+      const int blk = jb.int8 ? GEMM_BLK8 : GEMM_BLK4;
+      const int box = jb.n <= 16 ? 0 : jb.n <= 32 ? 1 : 2;
+      const bool lo = jb.lomap >= 0;
+      const uint32_t tx = (uint32_t)(blk + SUMS_BYTES) + (16u << box) * 128u * (lo ? 2u : 1u);
+      // lane 0: the weight block and B hi; lane 1: the K-tile's sums for the tile's rows (SUM_RUN floats from
+      // the first row rounded down to a multiple of 4: 16-byte aligned, the row strides being multiples of 4
+      // floats) and B lo
+      const uint8_t* bsrc = lane == 0 ? jb.w : reinterpret_cast<const uint8_t*>(jb.sum + (jb.row0 & ~3));
+      const size_t bstep = lane == 0 ? (size_t)blk : (size_t)jb.sstride * 4;
+      const uint32_t bbytes = lane == 0 ? (uint32_t)blk : (uint32_t)SUMS_BYTES;
+      const CUtensorMap* map = &g.maps.m[lane == 1 && lo ? jb.lomap : jb.bmap][box];
+      const bool tload = lane == 0 || (lane == 1 && lo);
+      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sr.next(NSG)) {
+        if ((gk & 1u) != par) continue;
+        const int s = sr.t;
+        const bool ok = gk < NSG || wait(&bar->empty[s], sr.ph ^ 1u);
+        if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
+        if (withhold && gk == 0) continue;
+        uint8_t* st = smem + s * geo.bytes;
+        if (lane == 0) mbar_expect_tx(&bar->full[s], tx);
+        __syncwarp();
+        if (lane < 2)
+          bulk_g2s(lane == 0 ? st + ST_W : reinterpret_cast<uint8_t*>(sums + s * SUM_RUN), bsrc + kt * bstep,
+                   bbytes, &bar->full[s]);
+        if (tload) tma_load_2d(st + (lane == 0 ? geo.bhi : geo.blo), map, kt * 64, jb.row0, &bar->full[s]);
+        if (lane == 0) GSTAMP(0, gk);
       }
-      // drain: every copy issued must have landed before the CTA leaves (the withheld one was never issued)
+    }
+    // drain: every copy this warp issued must have landed before the CTA leaves (the withheld one was never
+    // issued); only the last NSG K-tiles can still be in flight
+    if (lane == 0) {
       const uint32_t cnt = gk < (uint32_t)NSG ? gk : (uint32_t)NSG;
       for (uint32_t q = gk - cnt; q < gk; ++q)
-        if (!(withhold && q == 0)) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
+        if ((q & 1u) == par && !(withhold && q == 0)) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 14) {
@@ -276,29 +320,29 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       uint32_t gk = 0;
       bool run = true;
       JobIter it;
-      job_begin(g, it);
+      job_begin(g, ngroups, tw, it);
       Job jb;
-      SlotRing sl;
+      SlotRing sl, sr;
       while (run && job_next(g, it, jb)) {
         const uint32_t idesc = umma_idesc_f16(128, jb.n);
         const bool lo = jb.lomap >= 0;
-        for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt)) {
+        for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
           if ((gk & 1u) != par) continue;
-          const int s = gk % NSG, t = sl.t;
+          const int s = sr.t, t = sl.t;
           // a_ready implies full[s] and that the fold of K-tile gk - nt released slot t (the dequantisation
           // waited for both)
           if (!wait(&bar->a_ready[t], sl.ph)) { run = false; break; }
           GSTAMP(6, gk);
           tc_fence_after();
           // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
-          const uint8_t* st = smem + s * ST_BYTES;
-          const uint64_t bh = umma_desc_sw128(smem_u32(st + ST_BHI)), bl = umma_desc_sw128(smem_u32(st + ST_BLO));
+          const uint8_t* st = smem + s * geo.bytes;
+          const uint64_t bh = umma_desc_sw128(smem_u32(st + geo.bhi)), bl = umma_desc_sw128(smem_u32(st + geo.blo));
           const uint32_t d = tmem + t * slot_cols, a = d + a_col;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, ks > 0 ? 1u : 0u);
           if (lo)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d + TM_LO, a + 8 * ks, bl + 2 * ks, idesc, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d + tlo, a + 8 * ks, bl + 2 * ks, idesc, ks > 0 ? 1u : 0u);
           umma_commit(&bar->empty[s]);
           GSTAMP(3, gk);
         }
@@ -317,41 +361,27 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     uint32_t gk = 0;
     bool run = true;
     JobIter it;
-    job_begin(g, it);
+    job_begin(g, ngroups, tw, it);
     Job jb;
-    SlotRing sl;
+    SlotRing sl, sr;
     while (run && job_next(g, it, jb)) {
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt)) {
+      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
         if ((int)(gk & 1u) != grp) continue;
-        const int s = gk % NSG, t = sl.t;
+        const int s = sr.t, t = sl.t;
         // d_free[t] of K-tile gk - nt: the fold is done with slot t, and the MMAs that read its A are complete
-        if (!wait(&bar->full[s], (gk / NSG) & 1u) ||
+        if (!wait(&bar->full[s], sr.ph) ||
             (gk >= (uint32_t)nt && !wait(&bar->d_free[t], sl.ph ^ 1u))) {
           run = false;
           break;
         }
         if (r == 0) GSTAMP(1, gk);
-        const uint8_t* st = smem + s * ST_BYTES + ST_W;
-        // the fold's share of the stage goes to the side buffer, so the stage is free once the MMA has read B
+        const uint8_t* st = smem + s * geo.bytes + ST_W;
+        // the fold's share of the stage goes to the side buffer, so the stage is free once the MMA has read B:
+        // row r's (s, b) pair and the sums of the tile's activation rows
         {
           uint32_t* side = reinterpret_cast<uint32_t*>(smem + S_SIDE + t * SIDE_BYTES);
           side[r] = *reinterpret_cast<const uint32_t*>(st + 128 * (jb.int8 ? 64 : 32) + r * 4);
-          // sums of the tile's activation rows over its 64 columns (low halves / 4096): one (row, 16-byte
-          // chunk) item per thread, the 8 chunks of a row on 8 neighbouring lanes. jb.n * 8 is a multiple of
-          // 128, so every warp of the group runs the same iterations.
-          const uint8_t* bst = smem + s * ST_BYTES;
-          float* xsum = reinterpret_cast<float*>(side) + 128;
-#pragma unroll 1
-          for (int i = r; i < jb.n * 8; i += 128) {
-            const int row = i >> 3, c = i & 7;
-            const uint32_t off = sw128_off(row, c);
-            float tot = sum8_h(*reinterpret_cast<const uint4*>(bst + ST_BHI + off));
-            if (jb.lomap >= 0) tot = fmaf(sum8_h(*reinterpret_cast<const uint4*>(bst + ST_BLO + off)), 1.0f / 4096.0f, tot);
-            tot += __shfl_xor_sync(0xFFFFFFFFu, tot, 1);
-            tot += __shfl_xor_sync(0xFFFFFFFFu, tot, 2);
-            tot += __shfl_xor_sync(0xFFFFFFFFu, tot, 4);
-            if (c == 0) xsum[row] = tot;
-          }
+          if (r < CHUNK_NT) reinterpret_cast<float*>(side)[128 + r] = sums[s * SUM_RUN + (jb.row0 & 3) + r];
         }
         // row r of A in K order: column 4c + k of the slot holds the fp16 pair k of 8-column block c
         uint32_t arow[32];
@@ -415,18 +445,18 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     uint32_t gk = 0;
     bool run = true;
     JobIter it;
-    job_begin(g, it);
+    job_begin(g, ngroups, tw, it);
     Job jb;
-    SlotRing sl;
+    SlotRing sl, sr;
     while (run && job_next(g, it, jb)) {
       float acc[CHUNK_NT];
 #pragma unroll
       for (int i = 0; i < CHUNK_NT; ++i) acc[i] = 0.f;
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt)) {
-        const int s = gk % NSG, t = sl.t;
+      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
+        const int s = sr.t, t = sl.t;
         // empty[s] completes once the MMAs have finished and the dequantisation (which wrote the side buffer
         // before arriving) is done
-        if (!wait(&bar->empty[s], (gk / NSG) & 1u)) {
+        if (!wait(&bar->empty[s], sr.ph)) {
           run = false;
           break;
         }
@@ -436,20 +466,26 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         const float2 sb = h2f(side[r]);
         const float4* xs4 = reinterpret_cast<const float4*>(side + 128);
         const uint32_t d = trow + t * slot_cols;
+        const float slo = sb.x * (1.0f / 4096.0f);
+        // 16 columns at a time; the low-half accumulator after the high one, so that one 16-register buffer
+        // serves both (the 64 accumulators stay in registers)
 #pragma unroll
         for (int c0 = 0; c0 < CHUNK_NT; c0 += 16) {
           if (c0 < jb.n) {
-            uint32_t vh[16], vl[16];
-            tmem_ld16_nowait(d + c0, vh);
-            if (jb.lomap >= 0) tmem_ld16_nowait(d + TM_LO + c0, vl);
+            uint32_t v[16];
+            tmem_ld16_nowait(d + c0, v);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float dv = __uint_as_float(vh[i]);
-              if (jb.lomap >= 0) dv = fmaf(__uint_as_float(vl[i]), 1.0f / 4096.0f, dv);
               const float4 x4 = xs4[(c0 + i) >> 2];
               const float xv = (i & 3) == 0 ? x4.x : (i & 3) == 1 ? x4.y : (i & 3) == 2 ? x4.z : x4.w;
-              acc[c0 + i] = fmaf(sb.x, dv, fmaf(sb.y, xv, acc[c0 + i]));
+              acc[c0 + i] = fmaf(sb.x, __uint_as_float(v[i]), fmaf(sb.y, xv, acc[c0 + i]));
+            }
+            if (jb.lomap >= 0) {
+              tmem_ld16_nowait(d + tlo + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(slo, __uint_as_float(v[i]), acc[c0 + i]);
             }
           }
         }
@@ -481,21 +517,32 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         for (int i = 0; i < cnt; ++i) dst[(size_t)(jb.row0 + i) * G.H + jb.m * 128 + r] = ep[r * 65 + i];
       } else {
         // SwiGLU: rows 0-63 are gate units 64m.., rows 64-127 the matching up units. h = silu(g) * u is split
-        // into fp16 hi + lo/4096 halves, the down projection's B operand. Thread = (unit u, token parity).
+        // into fp16 hi + lo/4096 halves, the down projection's B operand; the 64 units are group m of the down
+        // projection's reduction, so the group's sum (of hi + lo/4096, the values the MMAs see) is made here
+        // too. Warp = token (4 at a time), lane = units u and u + 32.
         const bool sh = jb.kind == GK_SHGU;
         const int kd = sh ? G.Is : G.I;
         uint16_t* dhi = sh ? S.hs : S.hh;
         uint16_t* dlo = sh ? S.hs_lo : S.hh_lo;
-        const int u = r & 63;
-        const int pos = p8u(jb.m * 64 + u);
-#pragma unroll 2
-        for (int i = r >> 6; i < cnt; i += 2) {
-          const float h = silu_c(ep[u * 65 + i]) * ep[(u + 64) * 65 + i];
-          const __half hh = __float2half_rn(h);
-          const __half hl = __float2half_rn((h - __half2float(hh)) * 4096.0f);
-          const size_t o = (size_t)(jb.row0 + i) * kd + pos;
-          dhi[o] = __half_as_ushort(hh);
-          dlo[o] = __half_as_ushort(hl);
+        float* dsum = (sh ? S.sum_hs : S.sum_hh) + (size_t)jb.m * (sh ? S.sp : S.sr);
+        const int pos0 = p8u(jb.m * 64 + lane), pos1 = p8u(jb.m * 64 + 32 + lane);
+#pragma unroll 1
+        for (int i = q4; i < cnt; i += 4) {
+          float part = 0.f;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int u = lane + 32 * hf;
+            const float h = silu_c(ep[u * 65 + i]) * ep[(u + 64) * 65 + i];
+            const __half hh = __float2half_rn(h);
+            const __half hl = __float2half_rn((h - __half2float(hh)) * 4096.0f);
+            const size_t o = (size_t)(jb.row0 + i) * kd + (hf ? pos1 : pos0);
+            dhi[o] = __half_as_ushort(hh);
+            dlo[o] = __half_as_ushort(hl);
+            part += fmaf(__half2float(hl), 1.0f / 4096.0f, __half2float(hh));
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+          if (lane == 0) dsum[jb.row0 + i] = part;
         }
       }
       if (!fold_sync()) break;   // the staging buffer is free for the next job

@@ -10,6 +10,7 @@
 #include <stdio.h>
 
 #include "../../include/moe_block.h"
+#include "topk.cuh"
 
 namespace {
 
@@ -45,35 +46,16 @@ __global__ void k_na_logits(const uint8_t* __restrict__ q, const uint16_t* __res
 }
 
 // softmax over the E expert logits -> the k largest (lower index on ties) -> renormalise; sigmoid of logit E.
-// One warp per token; ids ascending.
+// One warp per token; ids ascending, each below E whatever the logits hold. EPL: logits per lane, 32 * EPL >= E.
+template <int EPL>
 __global__ void k_na_topk(const float* __restrict__ logits, int E, int K, int T, int32_t* __restrict__ ids,
                           float* __restrict__ w, float* __restrict__ sg) {
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* lg = logits + (size_t)t * (E + 1);
-  float v[NA_MAX_E / 32];
-  const int epl = (E + 31) / 32;
-  for (int i = 0; i < NA_MAX_E / 32; ++i) {
-    const int e = lane * epl + i;
-    v[i] = (i < epl && e < E) ? lg[e] : -INFINITY;
-  }
-  int sel_idx = -1;
-  float sel_val = 0.f;
-  for (int j = 0; j < K; ++j) {
-    float best = -INFINITY;
-    int bi = 0;
-    for (int i = 0; i < NA_MAX_E / 32; ++i)
-      if (v[i] > best) { best = v[i]; bi = i; }
-    int best_e = best == -INFINITY ? 0x7FFFFFFF : lane * epl + bi;
-    float m = best;
-    for (int o = 16; o > 0; o >>= 1) {
-      const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      const int oe = __shfl_xor_sync(0xFFFFFFFFu, best_e, o);
-      if (om > m || (om == m && oe < best_e)) { m = om; best_e = oe; }
-    }
-    if (best_e == lane * epl + bi && best == m) v[bi] = -INFINITY;
-    if (lane == j) { sel_idx = best_e; sel_val = m; }
-  }
+  int sel_idx;
+  float sel_val;
+  moe::warp_topk_lean<EPL, false>(lg, E, K, sel_idx, sel_val);
   const float mx = __shfl_sync(0xFFFFFFFFu, sel_val, 0);
   const float ex = lane < K ? expf(sel_val - mx) : 0.f;
   float z = ex;
@@ -116,6 +98,8 @@ extern "C" int moe_router_topk_noalloc(const uint8_t* router_q, const uint16_t* 
   const int rows = n_experts + 1;
   k_na_logits<<<(rows + 7) / 8, 256, 0, st>>>(router_q, router_s, router_b, hidden, n_experts,
                                                (const uint16_t*)x, T, scratch);
-  k_na_topk<<<(T + 7) / 8, 256, 0, st>>>(scratch, n_experts, top_k, T, ids, weights, sgate);
+  auto* topk = n_experts <= 32 ? k_na_topk<1> : n_experts <= 64 ? k_na_topk<2> : n_experts <= 128 ? k_na_topk<4>
+               : n_experts <= 256 ? k_na_topk<8> : k_na_topk<16>;
+  topk<<<(T + 7) / 8, 256, 0, st>>>(scratch, n_experts, top_k, T, ids, weights, sgate);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
