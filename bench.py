@@ -80,10 +80,14 @@ def traffic_record():
     return d.get("dram_bytes_per_launch")
 
 
+# k_decode1's sources
+KERNEL_SOURCES = ("decode1.cu", "decode_dev.cuh", "topk.cuh", "decode.cuh", "layout.cuh", "ptx.cuh")
+
+
 def kernel_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a16_top_mixture_gb300", "csrc")
-    for f in ("decode1.cu", "decode_dev.cuh", "decode.cuh", "layout.cuh", "ptx.cuh"):   # k_decode1's sources
+    for f in KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
