@@ -24,6 +24,7 @@ struct moe_block {
   bool loaded = false, has_gamma = false;
   int dec_T = 0;                                   // largest T the decode scratch holds
   float *logits = nullptr, *hs = nullptr, *hbuf = nullptr;
+  uint64_t* xlog = nullptr;
   uint32_t *counters = nullptr, *status = nullptr;
   int32_t* rec_ids = nullptr;
   float *rec_w = nullptr, *rec_sg = nullptr;
@@ -80,6 +81,7 @@ static void free_all(moe_block* b) {
   cudaFree(b->wstore);
   cudaFree(b->gamma);
   cudaFree(b->logits);
+  cudaFree(b->xlog);
   cudaFree(b->hs);
   cudaFree(b->hbuf);
   cudaFree(b->counters);
@@ -189,6 +191,9 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   const int T = b->dec_T;
   if (e == cudaSuccess) e = cudaMalloc(&b->gamma, (size_t)c.hidden * 2);
   if (e == cudaSuccess) e = cudaMalloc(&b->logits, (size_t)T * (c.n_experts + 1) * 4);
+  // tags start at 0 and the first launch publishes epoch 1, so nothing stale is ever taken for fresh
+  if (e == cudaSuccess) e = cudaMalloc(&b->xlog, XLOG_COPIES * xlog_stride(c.n_experts) * 8);
+  if (e == cudaSuccess) e = cudaMemset(b->xlog, 0, XLOG_COPIES * xlog_stride(c.n_experts) * 8);
   if (e == cudaSuccess) e = cudaMalloc(&b->hs, (size_t)T * c.shared_inter * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->hbuf, decode_hbuf_floats(L, T) * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->counters, 8 * 4);
@@ -296,7 +301,7 @@ static DecodeArgs decode_args(moe_block* b, const uint16_t* x, uint16_t* out, ui
   a.gamma = gamma;
   a.eps = eps;
   a.T = T;
-  a.logits = b->logits; a.hs = b->hs; a.hbuf = b->hbuf;
+  a.logits = b->logits; a.xlog = b->xlog; a.hs = b->hs; a.hbuf = b->hbuf;
   a.counters = b->counters; a.status = b->status;
   a.rec_ids = b->rec_ids + (size_t)t0 * b->cfg.top_k;
   a.rec_w = b->rec_w + (size_t)t0 * b->cfg.top_k;
@@ -389,7 +394,9 @@ extern "C" int moe_block_get_status(moe_block_t* b, uint32_t* flags) {
   CK(cudaMemcpy(&st, b->status, 4, cudaMemcpyDeviceToHost));
   if (flags) *flags = st;
   if (st) {
-    CK(cudaMemset(b->counters, 0, 8 * 4));
+    // the counts and the status word; the single-token epoch (word 5) keeps counting, so that no word published
+    // before the reset can pass for a later launch's
+    CK(cudaMemset(b->counters, 0, 5 * 4));
     CK(cudaDeviceSynchronize());
     if (b->status_host) *b->status_host = 0;
     return MOE_ERR_DEVICE_TIMEOUT;

@@ -22,6 +22,10 @@ enum : uint32_t {
   ERR_WAIT_ROUTE = 32u, ERR_SEGMENTS = 64u,
 };
 
+// copies of the single-token kernel's published router logits (each CTA polls one), 256-byte aligned apart
+constexpr int XLOG_COPIES = 16;
+__host__ __device__ constexpr size_t xlog_stride(int E) { return (size_t)((E + 1 + 31) & ~31); }
+
 struct DecodeArgs {
   const uint8_t *router, *sh_gu, *sh_dn, *ex_gu, *ex_dn;
   const uint16_t* x;        // [T][H] fp16 (h_in in residual mode)
@@ -30,10 +34,12 @@ struct DecodeArgs {
   const uint16_t* gamma;    // non-null: residual mode, x_hat = RMSNorm(x), out = x + block(x_hat)
   float eps;
   int T;
-  float* logits;            // [T][E+1]
+  float* logits;            // [T][E+1] (the single-token kernel writes it only as CTA 0's record)
+  uint64_t* xlog;           // [XLOG_COPIES][xlog_stride(E)] the single-token kernel's router logits, published
+                            // as {logit, epoch} words, every copy alike
   float* hs;                // [T][Is]
   float* hbuf;              // [T*K][I] routed h, one row per (expert, token) pair in expert-sorted order
-  uint32_t* counters;       // [4]
+  uint32_t* counters;       // [8]: 0-3 exchange and exit counts, 4 the status word, 5 the single-token epoch
   uint32_t* status;
   int32_t* rec_ids;         // routing record [T][K] (written by CTA 0)
   float* rec_w;             // [T][K]

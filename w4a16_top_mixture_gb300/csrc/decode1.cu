@@ -217,15 +217,10 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
       if (!ok) set_error1(a, ctl, ERR_WAIT_ROUTE);
       if (ctl->abort) ok = false;
       stamp1(a, 17);
+      // the routing warp has issued the routed gate/up copies (before its arrival); they are drained here too
       const int np = ok ? ctl->npiece : 0;
 #pragma unroll 1
-      for (int i = 0; i < np; ++i) {
-        const int e = ctl->eid[ctl->piece_slot[i]];
-        copy_in(&ctl->bar[B_GU + i], gur + ctl->piece_off[i],
-                a.ex_gu + (size_t)e * L.exgu_expert + (size_t)ctl->piece_u0[i] * L.EU,
-                (uint32_t)((ctl->piece_u1[i] - ctl->piece_u0[i]) * L.EU), pol);
-        armed |= 1u << (B_GU + i);
-      }
+      for (int i = 0; i < np; ++i) armed |= 1u << (B_GU + i);
       if (MOE_PDL_AT == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       stamp1(a, 18);
       // the routed down rows overlay the router and shared gate/up regions: wait until every warp is done
@@ -255,6 +250,9 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     const int ctid = threadIdx.x - 32;
     // x, logits, counters, hs, h and out may belong to the previous launch until it has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // this launch's epoch: the router logits are published tagged with it (the previous launch's last CTA
+    // advanced the count)
+    const uint32_t ep = __ldcg(a.counters + 5) + 1u;
     if (ctid == 0) stamp1(a, 1);
 
     // ---- prologue: (RMSNorm ->) fp16 activations in pair order and per-chunk pair-column sums
@@ -314,11 +312,15 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
           const DotR<4, 1> d = dot_rows<H, 4, 1, true>(b0, b1, b2, b3, b0 + H, b1 + H, b2 + H, b3 + H, nr, x16, xsc,
                                                        0, 0, 1);
           if (lane == 0) stamp1(a, 28);
-          if (lane < nr) a.logits[ra + lane] = lane == 0 ? d.v[0][0] : lane == 1 ? d.v[0][1] : lane == 2 ? d.v[0][2] : d.v[0][3];
-          __syncwarp();
+          // one {logit, epoch} word per row and copy: a reader that sees the tag has the value. Lane c writes
+          // copy c (test hook: CTA 0 never publishes, so every reader's bounded wait runs out)
+          if (lane < XLOG_COPIES && !(a.skip_arrive && ra == 0)) {
+            uint64_t* dst = a.xlog + (size_t)lane * xlog_stride(E) + ra;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (i < nr) st_relaxed_u64(dst + i, ((uint64_t)ep << 32) | __float_as_uint(d.v[0][i]));
+          }
           if (lane == 0) stamp1(a, 25);
-          if (lane == 0 && !(a.skip_arrive && ra == 0)) red_release_add(&a.counters[0], (uint32_t)nr);
-          if (lane == 0) stamp1(a, 26);
         }
       }
     }
@@ -351,15 +353,64 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->bar[B_RFREE]);
 
-    // ---- R: routing (warp 0): all E+1 logits -> top-k, softmax weights, sigmoid gate, the CTA's plan
+    // ---- R: routing (warp 0): all E+1 logits -> top-k, softmax weights, sigmoid gate, the CTA's plan; the warp
+    // issues the CTA's routed gate/up copies itself, one lane per copy
     if (cw == 0) {
-      if (lane == 0 && !ctl->abort && !spin_geq(&a.counters[0], (uint32_t)(E + 1), a.timeout_ns))
-        set_error1(a, ctl, ERR_WAIT_LOGITS);
+      constexpr int EPL = (E + 31) / 32;
+      // poll the tagged logits until every one carries this launch's epoch; lane l holds experts l*EPL..,
+      // lane 0 also the shared-expert gate logit (row E). Each CTA polls one of the copies, so that the 152
+      // readers do not all queue on the same few cache lines.
+      uint32_t key[EPL];
+      float gl = 0.f;
+      bool got = false;
+      const uint64_t* xl = a.xlog + (size_t)(cta % XLOG_COPIES) * xlog_stride(E);
+      if (!warp_abort(ctl)) {
+        const uint64_t t0 = globaltimer();
+#pragma unroll 1
+        for (int round = 0;; ++round) {
+          if (round > 0) __nanosleep(64);
+          bool fresh = true;
+          if (E % 64 == 0 && EPL % 2 == 0) {
+#pragma unroll
+            for (int i = 0; i < EPL; i += 2) {
+              uint64_t w0, w1;
+              ld_relaxed_u64x2(xl + lane * EPL + i, w0, w1);
+              fresh = fresh && (uint32_t)(w0 >> 32) == ep && (uint32_t)(w1 >> 32) == ep;
+              key[i] = topk_key(__uint_as_float((uint32_t)w0));
+              key[i + 1] = topk_key(__uint_as_float((uint32_t)w1));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+              const int e = lane * EPL + i;
+              const uint64_t w = e < E ? ld_relaxed_u64(xl + e) : ((uint64_t)ep << 32);
+              fresh = fresh && (uint32_t)(w >> 32) == ep;
+              key[i] = e < E ? topk_key(__uint_as_float((uint32_t)w)) : 0u;
+            }
+          }
+          if (lane == 0) {
+            const uint64_t w = ld_relaxed_u64(xl + E);
+            fresh = fresh && (uint32_t)(w >> 32) == ep;
+            gl = __uint_as_float((uint32_t)w);
+          }
+          if (__all_sync(FULL, fresh)) { got = true; break; }
+          if (__shfl_sync(FULL, globaltimer() - t0 > a.timeout_ns || ctl->abort ? 1 : 0, 0)) break;
+        }
+        if (!got && lane == 0) set_error1(a, ctl, ERR_WAIT_LOGITS);
+      }
       __syncwarp();
       if (lane == 0) stamp1(a, 3);
+      // CTA 0 records the logits (the top-k consumes the keys)
+      if (cta == 0 && a.rec_ids) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+          if (lane * EPL + i < E) a.logits[lane * EPL + i] = topk_logit(key[i]);
+        if (lane == 0) a.logits[E] = gl;
+      }
       int my_idx = 0;
-      float my_logit = 0.f;
-      if (!warp_abort(ctl)) warp_topk_lean<(E + 31) / 32, E % 128 == 0>(a.logits, E, K, my_idx, my_logit);
+      uint32_t my_key = 0;
+      if (got) warp_topk_keys<EPL>(key, K, my_idx, my_key);
+      const float my_logit = topk_logit(my_key);
       const float mx = __shfl_sync(FULL, my_logit, 0);
       if (lane == 0) stamp1(a, 21);
       const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
@@ -370,41 +421,48 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
         ctl->eid[lane] = my_idx;
         ctl->wts[lane] = wv;
       }
-      if (lane == 0) ctl->sg = __frcp_rn(1.0f + __expf(-__ldcg(a.logits + E)));
-      if (cta == 0 && a.rec_ids && lane < K) {   // selection order; moe_block_debug_last_routing sorts it
-        a.rec_ids[lane] = my_idx;
-        a.rec_w[lane] = wv;
-      }
+      if (lane == 0) ctl->sg = __frcp_rn(1.0f + __expf(-gl));
       // the CTA's slice [ulo, uhi) of the K*I routed units (slot-major) in copies of at most PIECE_UNITS units
       // inside one expert: the slice covers at most two experts (the plan checks it), so copy k is, in closed
       // form, the k-th PIECE_UNITS-step of the first expert's part or then of the second's
       {
         const int js = ulo / I, cut = min(uhi, (js + 1) * I);
         const int n0 = cdiv(cut - ulo, PIECE_UNITS), n1 = cdiv(uhi - cut, PIECE_UNITS);
-        const int np = warp_abort(ctl) || uhi <= ulo ? 0 : n0 + n1;
+        const int np = !got || warp_abort(ctl) || uhi <= ulo ? 0 : n0 + n1;
+        const bool first = lane < n0;
+        const int b0 = first ? ulo : cut, k = first ? lane : lane - n0;
+        const int u = b0 + k * PIECE_UNITS, u1 = min(first ? cut : uhi, u + PIECE_UNITS);
+        const int j = lane < np ? u / I : 0;
+        const int e = __shfl_sync(FULL, my_idx, j);   // the expert in selection slot j
         if (lane < np) {
-          const bool first = lane < n0;
-          const int b0 = first ? ulo : cut, k = first ? lane : lane - n0;
-          const int u = b0 + k * PIECE_UNITS, u1 = min(first ? cut : uhi, u + PIECE_UNITS);
-          const int j = u / I;
           ctl->piece_slot[lane] = j;
           ctl->piece_u0[lane] = u - j * I;
           ctl->piece_u1[lane] = u1 - j * I;
           ctl->piece_off[lane] = (u - ulo) * (int)L.EU;
           // unit pairs before this copy: whole first-part copies hold PIECE_UNITS / 2 pairs each
           ctl->piece_pair0[lane] = first ? k * (PIECE_UNITS / 2) : cdiv(cut - ulo, 2) + k * (PIECE_UNITS / 2);
+          copy_in(&ctl->bar[B_GU + lane], gur + (u - ulo) * (int)L.EU,
+                  a.ex_gu + (size_t)e * L.exgu_expert + (size_t)(u - j * I) * L.EU, (uint32_t)((u1 - u) * L.EU),
+                  policy_evict_first());
         }
         if (lane == 0) {
           ctl->piece_pair0[np] = np == 0 ? 0 : cdiv(cut - ulo, 2) + cdiv(uhi - cut, 2);
           ctl->npiece = np;
           ctl->npair = np == 0 ? 0 : cdiv(cut - ulo, 2) + cdiv(uhi - cut, 2);
-          if (cta == 0 && a.rec_sg) a.rec_sg[0] = ctl->sg;
         }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&ctl->bar[B_ROUTE]);
           stamp1(a, 4);
         }
+      }
+      // CTA 0's routing record (selection order; moe_block_debug_last_routing sorts it)
+      if (cta == 0 && a.rec_ids) {
+        if (lane < K) {
+          a.rec_ids[lane] = my_idx;
+          a.rec_w[lane] = wv;
+        }
+        if (lane == 0 && a.rec_sg) a.rec_sg[0] = ctl->sg;
       }
     }
 
@@ -574,6 +632,7 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     const uint32_t prev = atomicAdd(&a.counters[3], 1u);
     if (prev == (uint32_t)G - 1) {
       a.counters[0] = 0; a.counters[1] = 0; a.counters[2] = 0;
+      a.counters[5] = __ldcg(a.counters + 5) + 1u;   // the next launch's epoch is one more than this one's
       __threadfence();
       a.counters[3] = 0;
     }

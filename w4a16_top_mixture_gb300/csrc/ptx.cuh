@@ -105,6 +105,19 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// 64-bit relaxed accesses at GPU scope. A naturally aligned 64-bit access is single-copy atomic, so a word that
+// carries a value and a tag is seen whole or not at all (each element of the two-word load on its own).
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void ld_relaxed_u64x2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
 // *cnt += v with release semantics at GPU scope: every write this thread made before (and every write it has
 // observed, e.g. through a preceding barrier) is visible to a thread that later reads the new count with an
 // acquire load (ld_acquire_u32). One instruction in place of a full fence followed by an atomic.
