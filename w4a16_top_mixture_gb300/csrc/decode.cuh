@@ -23,7 +23,10 @@ enum : uint32_t {
 };
 
 // copies of the single-token kernel's published router logits (each CTA polls one), 256-byte aligned apart
-constexpr int XLOG_COPIES = 16;
+#ifndef MOE_XLOG_COPIES
+#define MOE_XLOG_COPIES 16
+#endif
+constexpr int XLOG_COPIES = MOE_XLOG_COPIES;
 __host__ __device__ constexpr size_t xlog_stride(int E) { return (size_t)((E + 1 + 31) & ~31); }
 
 struct DecodeArgs {

@@ -368,7 +368,10 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
         const uint64_t t0 = globaltimer();
 #pragma unroll 1
         for (int round = 0;; ++round) {
-          if (round > 0) __nanosleep(64);
+#ifndef MOE_POLL_NS
+#define MOE_POLL_NS 64
+#endif
+          if (MOE_POLL_NS > 0 && round > 0) __nanosleep(MOE_POLL_NS);
           bool fresh = true;
           if (E % 64 == 0 && EPL % 2 == 0) {
 #pragma unroll
@@ -410,21 +413,10 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
       int my_idx = 0;
       uint32_t my_key = 0;
       if (got) warp_topk_keys<EPL>(key, K, my_idx, my_key);
-      const float my_logit = topk_logit(my_key);
-      const float mx = __shfl_sync(FULL, my_logit, 0);
-      if (lane == 0) stamp1(a, 21);
-      const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
-      const float Z = warp_sum(ex);
-      const float wv = __fdividef(ex, Z);
-      if (lane == 0) stamp1(a, 22);
-      if (lane < K) {
-        ctl->eid[lane] = my_idx;
-        ctl->wts[lane] = wv;
-      }
-      if (lane == 0) ctl->sg = __frcp_rn(1.0f + __expf(-gl));
       // the CTA's slice [ulo, uhi) of the K*I routed units (slot-major) in copies of at most PIECE_UNITS units
       // inside one expert: the slice covers at most two experts (the plan checks it), so copy k is, in closed
-      // form, the k-th PIECE_UNITS-step of the first expert's part or then of the second's
+      // form, the k-th PIECE_UNITS-step of the first expert's part or then of the second's. The copies need only
+      // the selected experts: they go out first, the softmax weights (read at the very end) after them.
       {
         const int js = ulo / I, cut = min(uhi, (js + 1) * I);
         const int n0 = cdiv(cut - ulo, PIECE_UNITS), n1 = cdiv(uhi - cut, PIECE_UNITS);
@@ -434,6 +426,10 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
         const int u = b0 + k * PIECE_UNITS, u1 = min(first ? cut : uhi, u + PIECE_UNITS);
         const int j = lane < np ? u / I : 0;
         const int e = __shfl_sync(FULL, my_idx, j);   // the expert in selection slot j
+        if (lane < np)
+          copy_in(&ctl->bar[B_GU + lane], gur + (u - ulo) * (int)L.EU,
+                  a.ex_gu + (size_t)e * L.exgu_expert + (size_t)(u - j * I) * L.EU, (uint32_t)((u1 - u) * L.EU),
+                  policy_evict_first());
         if (lane < np) {
           ctl->piece_slot[lane] = j;
           ctl->piece_u0[lane] = u - j * I;
@@ -441,10 +437,8 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
           ctl->piece_off[lane] = (u - ulo) * (int)L.EU;
           // unit pairs before this copy: whole first-part copies hold PIECE_UNITS / 2 pairs each
           ctl->piece_pair0[lane] = first ? k * (PIECE_UNITS / 2) : cdiv(cut - ulo, 2) + k * (PIECE_UNITS / 2);
-          copy_in(&ctl->bar[B_GU + lane], gur + (u - ulo) * (int)L.EU,
-                  a.ex_gu + (size_t)e * L.exgu_expert + (size_t)(u - j * I) * L.EU, (uint32_t)((u1 - u) * L.EU),
-                  policy_evict_first());
         }
+        if (lane < K) ctl->eid[lane] = my_idx;
         if (lane == 0) {
           ctl->piece_pair0[np] = np == 0 ? 0 : cdiv(cut - ulo, 2) + cdiv(uhi - cut, 2);
           ctl->npiece = np;
@@ -456,6 +450,16 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
           stamp1(a, 4);
         }
       }
+      // softmax over the selected logits (selection order), the shared expert's sigmoid gate
+      const float my_logit = topk_logit(my_key);
+      const float mx = __shfl_sync(FULL, my_logit, 0);
+      if (lane == 0) stamp1(a, 21);
+      const float ex = lane < K ? __expf(my_logit - mx) : 0.f;
+      const float Z = warp_sum(ex);
+      const float wv = __fdividef(ex, Z);
+      if (lane == 0) stamp1(a, 22);
+      if (lane < K) ctl->wts[lane] = wv;
+      if (lane == 0) ctl->sg = __frcp_rn(1.0f + __expf(-gl));
       // CTA 0's routing record (selection order; moe_block_debug_last_routing sorts it)
       if (cta == 0 && a.rec_ids) {
         if (lane < K) {
