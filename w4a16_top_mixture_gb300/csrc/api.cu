@@ -196,8 +196,8 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
   if (e == cudaSuccess) e = cudaMemset(b->xlog, 0, XLOG_COPIES * xlog_stride(c.n_experts) * 8);
   if (e == cudaSuccess) e = cudaMalloc(&b->hs, (size_t)T * c.shared_inter * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->hbuf, decode_hbuf_floats(L, T) * 4);
-  if (e == cudaSuccess) e = cudaMalloc(&b->counters, 8 * 4);
-  if (e == cudaSuccess) e = cudaMemset(b->counters, 0, 8 * 4);
+  if (e == cudaSuccess) e = cudaMalloc(&b->counters, CNT_WORDS * 4);
+  if (e == cudaSuccess) e = cudaMemset(b->counters, 0, CNT_WORDS * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->rec_ids, (size_t)c.max_tokens * c.top_k * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->rec_w, (size_t)c.max_tokens * c.top_k * 4);
   if (e == cudaSuccess) e = cudaMalloc(&b->rec_sg, (size_t)c.max_tokens * 4);
@@ -221,7 +221,7 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
     delete b;
     return cuda_fail(e, "moe_block_create");
   }
-  b->status = b->counters + 4;
+  b->status = b->counters + CNT_STATUS;
   *out = b;
   return MOE_OK;
 }
@@ -394,9 +394,10 @@ extern "C" int moe_block_get_status(moe_block_t* b, uint32_t* flags) {
   CK(cudaMemcpy(&st, b->status, 4, cudaMemcpyDeviceToHost));
   if (flags) *flags = st;
   if (st) {
-    // the counts and the status word; the single-token epoch (word 5) keeps counting, so that no word published
-    // before the reset can pass for a later launch's
-    CK(cudaMemset(b->counters, 0, 5 * 4));
+    // every count, the status word and the single-token epoch, and the published logit tags with it (the next
+    // launch publishes epoch 1, which nothing left in the buffers carries)
+    CK(cudaMemset(b->counters, 0, CNT_WORDS * 4));
+    CK(cudaMemset(b->xlog, 0, XLOG_COPIES * xlog_stride(b->cfg.n_experts) * 8));
     CK(cudaDeviceSynchronize());
     if (b->status_host) *b->status_host = 0;
     return MOE_ERR_DEVICE_TIMEOUT;

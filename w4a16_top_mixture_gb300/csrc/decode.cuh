@@ -20,7 +20,13 @@ constexpr int DEC1_THREADS = (DEC1_NCW + 1) * 32; // + one producer warp
 enum : uint32_t {
   ERR_WAIT_LOGITS = 1u, ERR_WAIT_HS = 2u, ERR_WAIT_H = 4u, ERR_WAIT_FULL = 8u, ERR_WAIT_EMPTY = 16u,
   ERR_WAIT_ROUTE = 32u, ERR_SEGMENTS = 64u,
+  ERR_REFUSED = 128u,   // the single-token kernel found an earlier error not yet cleared and computed nothing
 };
+
+// Words of the handle's counter array (uint32 units). The multi-token kernel's counts (reset by its last CTA),
+// the status word, and the single-token kernel's epoch and its two 64-bit exchange counts, which only grow:
+// launch ep waits for ep * Is shared units and ep * K * I routed units.
+constexpr int CNT_STATUS = 4, CNT_EPOCH = 5, CNT_HS64 = 8, CNT_H64 = 10, CNT_WORDS = 16;
 
 // copies of the single-token kernel's published router logits (each CTA polls one), 256-byte aligned apart
 #ifndef MOE_XLOG_COPIES
@@ -42,7 +48,7 @@ struct DecodeArgs {
                             // as {logit, epoch} words, every copy alike
   float* hs;                // [T][Is]
   float* hbuf;              // [T*K][I] routed h, one row per (expert, token) pair in expert-sorted order
-  uint32_t* counters;       // [8]: 0-3 exchange and exit counts, 4 the status word, 5 the single-token epoch
+  uint32_t* counters;       // [CNT_WORDS], see CNT_*
   uint32_t* status;
   int32_t* rec_ids;         // routing record [T][K] (written by CTA 0)
   float* rec_w;             // [T][K]

@@ -250,9 +250,17 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     const int ctid = threadIdx.x - 32;
     // x, logits, counters, hs, h and out may belong to the previous launch until it has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // this launch's epoch: the router logits are published tagged with it (the previous launch's last CTA
-    // advanced the count)
-    const uint32_t ep = __ldcg(a.counters + 5) + 1u;
+    // this launch's epoch: the router logits are published tagged with it, and the exchange counts reach
+    // ep * expected (CTA 0 of the previous launch advanced it). A launch that finds an earlier error still set
+    // computes nothing: the counts and tags are consistent again only once the host has read and reset the
+    // status.
+    const uint32_t ep = __ldcg(a.counters + CNT_EPOCH) + 1u;
+    uint64_t* cnt_hs = reinterpret_cast<uint64_t*>(a.counters + CNT_HS64);
+    uint64_t* cnt_h = reinterpret_cast<uint64_t*>(a.counters + CNT_H64);
+    if (__ldcg(a.status) != 0u && ctid == 0) {
+      atomicOr(a.status, ERR_REFUSED);
+      ctl->abort = 1;
+    }
     if (ctid == 0) stamp1(a, 1);
 
     // ---- prologue: (RMSNorm ->) fp16 activations in pair order and per-chunk pair-column sums
@@ -346,7 +354,7 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
           }
         }
         __syncwarp();
-        if (lane == 0 && done > 0) red_release_add(&a.counters[1], (uint32_t)done);
+        if (lane == 0 && done > 0) red_release_add_u64(cnt_hs, (uint64_t)done);
       }
     }
     // this warp no longer reads the router or shared gate/up regions
@@ -400,6 +408,9 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
           if (__shfl_sync(FULL, globaltimer() - t0 > a.timeout_ns || ctl->abort ? 1 : 0, 0)) break;
         }
         if (!got && lane == 0) set_error1(a, ctl, ERR_WAIT_LOGITS);
+        // every CTA read the epoch before it published its rows, so once all rows carry it the next launch's
+        // epoch can be set: the next launch reads it only after this one has completed
+        if (got && cta == 0 && lane == 0) a.counters[CNT_EPOCH] = ep;
       }
       __syncwarp();
       if (lane == 0) stamp1(a, 3);
@@ -475,7 +486,7 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     if (cw >= CTW0) {
       const int ct = ctid - CTW0 * 32;
       if (ct == 0) stamp1(a, 23);
-      if (ct == 0 && !ctl->abort && !spin_geq(&a.counters[1], (uint32_t)Is, a.timeout_ns))
+      if (ct == 0 && !ctl->abort && !spin_geq_u64(cnt_hs, (uint64_t)ep * Is, a.timeout_ns))
         set_error1(a, ctl, ERR_WAIT_HS);
       named_bar(BAR_CT, 64);
       if (nrow > 0) wait_landed(a, ctl, &ctl->bar[B_PRE + 2]);
@@ -530,14 +541,14 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
         done += nu;
       }
       __syncwarp();
-      if (lane == 0 && done > 0) red_release_add(&a.counters[2], (uint32_t)done);
+      if (lane == 0 && done > 0) red_release_add_u64(cnt_h, (uint64_t)done);
       wstamp1(a, cw, 1);
     }
     named_bar(BAR_ALL, CT1);   // the CTA's gate/up region is no longer read
     if (ctid == 0) {
       stamp1(a, 5);
       if (MOE_PDL_AT == 2) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-      if (!ctl->abort && !spin_geq(&a.counters[2], (uint32_t)(K * I), a.timeout_ns)) set_error1(a, ctl, ERR_WAIT_H);
+      if (!ctl->abort && !spin_geq_u64(cnt_h, (uint64_t)ep * (K * I), a.timeout_ns)) set_error1(a, ctl, ERR_WAIT_H);
       stamp1(a, 6);
       if (!ctl->abort) {
         fence_proxy_async_global();
@@ -630,16 +641,6 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     else if (threadIdx.x < 32 + W1 * 4)
       a.trace[G * 32 + (cta * 16 + (threadIdx.x - 32) / 4) * 4 + (threadIdx.x - 32) % 4] =
           ctl->wclk[(threadIdx.x - 32) / 4][(threadIdx.x - 32) % 4];
-  }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(&a.counters[3], 1u);
-    if (prev == (uint32_t)G - 1) {
-      a.counters[0] = 0; a.counters[1] = 0; a.counters[2] = 0;
-      a.counters[5] = __ldcg(a.counters + 5) + 1u;   // the next launch's epoch is one more than this one's
-      __threadfence();
-      a.counters[3] = 0;
-    }
   }
 }
 

@@ -125,6 +125,30 @@ __device__ __forceinline__ void red_release_add(uint32_t* cnt, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(cnt), "r"(v) : "memory");
 }
 
+// 64-bit counts that only grow (the single-token kernel's exchange counts, compared with epoch * expected)
+__device__ __forceinline__ void red_release_add_u64(uint64_t* cnt, uint64_t v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(cnt), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+static __device__ __noinline__ bool spin_geq_u64_slow(const uint64_t* cnt, uint64_t target, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 8; ++i) {
+      if (ld_acquire_u64(cnt) >= target) return true;
+      __nanosleep(20);
+    }
+    if (globaltimer() - t0 > timeout_ns) return false;
+  }
+}
+__device__ __forceinline__ bool spin_geq_u64(const uint64_t* cnt, uint64_t target, uint64_t timeout_ns) {
+  if (ld_acquire_u64(cnt) >= target) return true;
+  return spin_geq_u64_slow(cnt, target, timeout_ns);
+}
+
 // Bounded spin until *cnt >= target. Returns false on timeout. The loop is out of line (one copy per kernel).
 static __device__ __noinline__ bool spin_geq_slow(const uint32_t* cnt, uint32_t target, uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer();
