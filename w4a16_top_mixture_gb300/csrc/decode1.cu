@@ -51,6 +51,7 @@ constexpr int W1 = DEC1_NCW;
 constexpr int CT1 = W1 * 32;
 constexpr int BAR_ALL = 1;           // every consumer warp
 constexpr int BAR_CT = 2;            // the shared-down team (two warps)
+constexpr int BAR_A1 = 3;            // the two router warps
 constexpr int MAXPIECE = 8;          // routed gate/up copies of one CTA
 constexpr int PIECE_UNITS = MOE_PIECE_UNITS;
 constexpr int A2W0 = 2;              // first warp of the shared gate/up work
@@ -76,6 +77,7 @@ struct Ctl1 {
   float wts[16];                     // their renormalised softmax weights
   float sg;                          // sigmoid of the shared-gate logit
   float rn;                          // 1 / RMS of the layer input (residual mode)
+  float a1p[4];                      // warp 1's half of the router rows' dot products
   unsigned long long tclk[32];       // phase stamps (SM clock), flushed to the trace buffer at exit
   unsigned long long wclk[W1][4];
 };
@@ -306,19 +308,38 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     named_bar(BAR_ALL, CT1);
     if (ctid == 0) stamp1(a, 2);
 
-    // ---- A1: the CTA's router rows (at most four) -> logits by warp 0, then one count of its rows
+    // ---- A1: the CTA's router rows (at most four) -> logits. Warps 0 and 1 (idle until routing) each take half
+    // of the rows' chunks; warp 1 hands its sums over in shared memory and warp 0 publishes them.
     {
       const int nr = rb - ra;
-      if (cw == 0 && nr > 0) {
+      constexpr int PR = (NCH + 31) / 32;            // chunk passes of a row (dot_rows' P)
+      constexpr int A1W = PR >= 2 ? 2 : 1;           // warps on the router rows
+      if (cw < A1W && nr > 0) {
         wait_landed(a, ctl, &ctl->bar[B_PRE]);
-        if (lane == 0) stamp1(a, 27);
-        if (!warp_abort(ctl)) {
+        if (lane == 0 && cw == 0) stamp1(a, 27);
+        const bool live = !warp_abort(ctl);
+        DotR<4, 1> d = {};
+        if (live) {
           const uint8_t* b0 = rtr;
           const uint8_t* b1 = rtr + (size_t)min(1, nr - 1) * L.RR;
           const uint8_t* b2 = rtr + (size_t)min(2, nr - 1) * L.RR;
           const uint8_t* b3 = rtr + (size_t)min(3, nr - 1) * L.RR;
-          const DotR<4, 1> d = dot_rows<H, 4, 1, true>(b0, b1, b2, b3, b0 + H, b1 + H, b2 + H, b3 + H, nr, x16, xsc,
-                                                       0, 0, 1);
+          d = dot_rows<H, 4, 1, true>(b0, b1, b2, b3, b0 + H, b1 + H, b2 + H, b3 + H, nr, x16, xsc, 0, 0, 1,
+                                      cw * PR / A1W, (cw + 1) * PR / A1W);
+        }
+        if (A1W > 1) {
+          // both warps reach the barrier whatever the abort flag says (it may change between their reads)
+          if (cw == 1 && lane == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ctl->a1p[i] = d.v[0][i];
+          }
+          named_bar(BAR_A1, 64);
+          if (cw == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d.v[0][i] += ctl->a1p[i];
+          }
+        }
+        if (cw == 0 && live) {
           if (lane == 0) stamp1(a, 28);
           // one {logit, epoch} word per row and copy: a reader that sees the tag has the value. Lane c writes
           // copy c (test hook: CTA 0 never publishes, so every reader's bounded wait runs out)

@@ -164,7 +164,8 @@ __device__ __forceinline__ float down_int8(uint4 w, float2 sb, const Act16& a) {
 // chunk = 16 bytes at chunk * 16); INT8 = true: lane-interleaved int8 rows (16-byte halves of chunk c = l + LW*p
 // at ((2p + half) * LW + l) * 16). Lane l covers the 32-column chunks c = l + LW*p. Activations: x16[((t*P + p)*4
 // + j)*LW + l] the uint4 of 8-column block j of chunk c for token t; xsc[(t*P + p)*LW + l] = (inv, sum of the
-// chunk's quantised values times inv). Returns the warp-reduced v[tt][r] in every lane. Inlined: an out-of-line
+// chunk's quantised values times inv). Only the chunks of p in [p0, p1) are covered (p1 < 0: every p), so that
+// warps can share a row. Returns the warp-reduced v[tt][r] in every lane. Inlined: an out-of-line
 // call would save and restore the caller's registers through local memory, which has almost no L1 behind it when
 // shared memory takes the whole carveout.
 template <int H, int NR, int TK, bool INT8>
@@ -172,7 +173,7 @@ __device__ __forceinline__ DotR<NR, TK> dot_rows(const uint8_t* r0, const uint8_
                                               const uint8_t* r3, const uint8_t* s0, const uint8_t* s1,
                                               const uint8_t* s2, const uint8_t* s3, int nvalid,
                                               const uint4* __restrict__ x16, const float2* __restrict__ xsc,
-                                              int ta, int tb, int nt) {
+                                              int ta, int tb, int nt, int p0 = 0, int p1 = -1) {
   constexpr int NCH = H / 32, LW = NCH < 32 ? NCH : 32, P = (NCH + 31) / 32;
   const int lane = threadIdx.x & 31;
   const uint8_t* rp[4] = {r0, r1, r2, r3};
@@ -187,7 +188,7 @@ __device__ __forceinline__ DotR<NR, TK> dot_rows(const uint8_t* r0, const uint8_
     for (int r = 0; r < NR; ++r) out.v[tt][r] = 0.f;
   if (lane < LW) {
 #pragma unroll 1
-    for (int p = 0; p < P; ++p) {
+    for (int p = p0; p < (p1 < 0 ? P : p1); ++p) {
       const int c = lane + LW * p;
       int lo[TK][NR], hi[TK][NR];
 #pragma unroll
