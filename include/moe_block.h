@@ -97,7 +97,11 @@ MOE_API int moe_block_load_weights(moe_block_t *blk, const moe_block_weights_t *
  * fits the device. A kernel of another stream, process or client that holds SMs while a forward runs can keep
  * some of its CTAs from starting: the others then wait, bounded (500 ms by default), and the call ends without
  * its result, which moe_block_get_status (and moe_block_forward_host, which reads the status itself) reports
- * as MOE_ERR_DEVICE_TIMEOUT. Run forward with the SMs to itself, or poll the status. */
+ * as MOE_ERR_DEVICE_TIMEOUT. Run forward with the SMs to itself, or poll the status.
+ *
+ * After such an error the handle's single-token (T = 1) kernel computes nothing, and leaves out unwritten, until
+ * moe_block_get_status has reported the error and reset the handle: its grid-wide counts and published routing
+ * words are consistent again only then. The refused call adds bit 128 to the status flags. */
 MOE_API int moe_block_forward(moe_block_t *blk, const void *x, void *out, int T, void *stream);
 
 /* Same computation with HOST buffers: copies x to the device, runs forward and copies out back, then
@@ -112,7 +116,10 @@ MOE_API int moe_block_forward_residual(moe_block_t *blk, const void *h_in, void 
 /* Waits for the stream of the handle's last forward call (that stream must still exist; work replayed from a
  * CUDA graph on another stream must be synchronised by the caller first), then returns MOE_OK, or
  * MOE_ERR_DEVICE_TIMEOUT if a bounded device-side wait ran out in any earlier call (the handle's device state
- * is then reset, so the next call starts clean). *flags (may be NULL) receives the raw device error bits. */
+ * is then reset, so the next call starts clean). *flags (may be NULL) receives the raw device error bits: 1 the
+ * router logits, 2 the shared-expert h, 4 the routed h, 8 a weight copy, 16 a shared-memory region, 32 the
+ * routing plan were not ready in time; 128 a single-token call found an earlier error not yet reset and computed
+ * nothing; 512 a prompt-chunk GEMM wait ran out. */
 MOE_API int moe_block_get_status(moe_block_t *blk, uint32_t *flags);
 
 /* ---- stacked decoder layers (notebook section 7: the decoder layer wraps the MoE block in RMSNorm and a

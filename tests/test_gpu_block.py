@@ -218,7 +218,8 @@ def test_invalid_calls(prod_block):
 
 def test_bounded_wait_reports_timeout_and_recovers():
     """A withheld arrival (host-set test flag) makes every CTA's bounded wait run out: the call ends, the
-    status reports the timeout, and the next call on the same handle is correct again. No GPU fault."""
+    status reports the timeout, and the next call on the same handle is correct again. A call made while the
+    error is still unread computes nothing. No GPU fault."""
     cfg = synth.TINY
     w, x = make_case(cfg, 1, 5)
     r = O.block_forward(w, x, cfg.top_k)
@@ -230,6 +231,19 @@ def test_bounded_wait_reports_timeout_and_recovers():
     s, flags = blk.status()
     assert s == -5 and (flags & 1), (s, flags)
     blk.set_wait(0, False)
+    out, _, _ = run(blk, x)
+    assert check_tol(out, r["out"])[0]
+    # an error left unread: the next single-token call computes nothing (bit 128, its output untouched) until
+    # the status read resets the handle
+    blk.set_wait(timeout_us=20000, skip_arrive=True)
+    blk.forward(xd)
+    blk.set_wait(0, False)
+    sentinel = torch.full_like(xd, 7.0)
+    blk.forward(xd, sentinel)
+    torch.cuda.synchronize()
+    assert (sentinel == 7.0).all()
+    s, flags = blk.status()
+    assert s == -5 and (flags & 1) and (flags & 128), (s, flags)
     out, _, _ = run(blk, x)
     assert check_tol(out, r["out"])[0]
     blk.close()
