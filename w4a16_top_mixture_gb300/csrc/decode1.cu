@@ -34,9 +34,11 @@
 #include "ptx.cuh"
 
 // Where the CTAs allow the next launch on the stream to start (griddepcontrol.launch_dependents): 0 at the
-// start, 1 once the routed gate/up copies are issued, 2 after the routed gate/up work.
+// start, 1 once the routed gate/up copies are issued, 2 after the routed gate/up work, 3 after the routed down
+// rows. At 2 the next launch's weight-only copies no longer compete with this launch's routed copies for HBM,
+// and still land before this launch ends (12.7 against 13.2 us per step at 1).
 #ifndef MOE_PDL_AT
-#define MOE_PDL_AT 1
+#define MOE_PDL_AT 2
 #endif
 // routed gate/up units per bulk copy (even, so a unit pair never straddles two copies)
 #ifndef MOE_PIECE_UNITS
@@ -77,7 +79,7 @@ struct Ctl1 {
   float wts[16];                     // their renormalised softmax weights
   float sg;                          // sigmoid of the shared-gate logit
   float rn;                          // 1 / RMS of the layer input (residual mode)
-  float a1p[4];                      // warp 1's half of the router rows' dot products
+  float a1p[3][4];                   // the other router warps' parts of the router rows' dot products
   unsigned long long tclk[32];       // phase stamps (SM clock), flushed to the trace buffer at exit
   unsigned long long wclk[W1][4];
 };
@@ -308,35 +310,61 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     named_bar(BAR_ALL, CT1);
     if (ctid == 0) stamp1(a, 2);
 
-    // ---- A1: the CTA's router rows (at most four) -> logits. Warps 0 and 1 (idle until routing) each take half
-    // of the rows' chunks; warp 1 hands its sums over in shared memory and warp 0 publishes them.
+    // ---- A1: the CTA's router rows (at most four) -> logits, on warps that are idle until routing: A1W warps,
+    // each half of a row set's chunks (with four warps, warps 0, 1 take rows 0 and 2 and warps 4, 5 rows 1 and
+    // 3). Warps other than 0 hand their sums over in shared memory and warp 0 publishes them.
     {
       const int nr = rb - ra;
       constexpr int PR = (NCH + 31) / 32;            // chunk passes of a row (dot_rows' P)
-      constexpr int A1W = PR >= 2 ? 2 : 1;           // warps on the router rows
-      if (cw < A1W && nr > 0) {
+#ifndef MOE_A1_WARPS
+#define MOE_A1_WARPS 2
+#endif
+      constexpr int A1W = PR >= 2 ? MOE_A1_WARPS : 1;   // warps on the router rows
+      static_assert(A1W == 1 || A1W == 2 || A1W == 4, "router warps");
+      const int aw = cw < 2 ? cw : cw - 2;               // index among the router warps (cw 0, 1, 4, 5)
+      const bool a1 = nr > 0 && (cw < (A1W < 2 ? A1W : 2) || (A1W == 4 && (cw == 4 || cw == 5)));
+      if (a1) {
         wait_landed(a, ctl, &ctl->bar[B_PRE]);
         if (lane == 0 && cw == 0) stamp1(a, 27);
         const bool live = !warp_abort(ctl);
         DotR<4, 1> d = {};
-        if (live) {
-          const uint8_t* b0 = rtr;
-          const uint8_t* b1 = rtr + (size_t)min(1, nr - 1) * L.RR;
-          const uint8_t* b2 = rtr + (size_t)min(2, nr - 1) * L.RR;
-          const uint8_t* b3 = rtr + (size_t)min(3, nr - 1) * L.RR;
-          d = dot_rows<H, 4, 1, true>(b0, b1, b2, b3, b0 + H, b1 + H, b2 + H, b3 + H, nr, x16, xsc, 0, 0, 1,
-                                      cw * PR / A1W, (cw + 1) * PR / A1W);
+        // this warp's rows: all of them with one or two warps; every other one with four (the pair index picks
+        // the first), compacted to the front of the call
+        const int pair = A1W == 4 ? aw >> 1 : 0, half = A1W == 1 ? 0 : (aw & 1);
+        const int step = A1W == 4 ? 2 : 1;
+        const int nv = A1W == 4 ? (nr - pair + 1) / 2 : nr;
+        if (live && nv > 0) {
+          const uint8_t* b0 = rtr + (size_t)min(pair, nr - 1) * L.RR;
+          const uint8_t* b1 = rtr + (size_t)min(pair + step, nr - 1) * L.RR;
+          const uint8_t* b2 = rtr + (size_t)min(pair + 2 * step, nr - 1) * L.RR;
+          const uint8_t* b3 = rtr + (size_t)min(pair + 3 * step, nr - 1) * L.RR;
+          d = dot_rows<H, 4, 1, true>(b0, b1, b2, b3, b0 + H, b1 + H, b2 + H, b3 + H, nv, x16, xsc, 0, 0, 1,
+                                      half * PR / (A1W == 1 ? 1 : 2), (half + 1) * PR / (A1W == 1 ? 1 : 2));
         }
         if (A1W > 1) {
-          // both warps reach the barrier whatever the abort flag says (it may change between their reads)
-          if (cw == 1 && lane == 0) {
+          // every router warp reaches the barrier whatever the abort flag says (it may change between reads)
+          if (aw != 0 && lane == 0) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ctl->a1p[i] = d.v[0][i];
+            for (int i = 0; i < 4; ++i) ctl->a1p[aw - 1][i] = d.v[0][i];
           }
-          named_bar(BAR_A1, 64);
+          named_bar(BAR_A1, 32 * A1W);
           if (cw == 0) {
+            // row pair * 1 + step * i of this warp's call i; with four warps warp 0 holds rows 0, 2 and the
+            // pair-1 warps rows 1, 3
+            float v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d.v[0][i] += ctl->a1p[i];
+            for (int i = 0; i < 4; ++i) v[i] = 0.f;
+            if (A1W == 2) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[i] = d.v[0][i] + ctl->a1p[0][i];
+            } else {
+              v[0] = d.v[0][0] + ctl->a1p[0][0];
+              v[2] = d.v[0][1] + ctl->a1p[0][1];
+              v[1] = ctl->a1p[1][0] + ctl->a1p[2][0];
+              v[3] = ctl->a1p[1][1] + ctl->a1p[2][1];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d.v[0][i] = v[i];
           }
         }
         if (cw == 0 && live) {
@@ -634,6 +662,7 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
     }
     named_bar(BAR_ALL, CT1);
     if (ctid == 0) stamp1(a, 8);
+    if (MOE_PDL_AT == 3 && ctid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- D: out = sum_j w_j y_j (selection order) + sigmoid(g) * shared row (+ residual), one fp16 rounding
     if (!ctl->abort) {
