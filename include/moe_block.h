@@ -77,6 +77,48 @@ typedef struct {
   const uint16_t *rms_gamma; /* may be NULL */
 } moe_block_weights_t;
 
+/* ---- affine checkpoint layout (TensorFold #3239, "Receipts": the block run from the published 4-bit affine
+ * checkpoint of Qwen3.6-35B-A3B). The pages name that checkpoint but give no layout; this loader reads the
+ * plainest one for group-64 affine tensors:
+ *   q       [rows][in * bits / 32] uint32 words along the input dimension, little-endian: with bits = 4 word c
+ *           holds inputs 8c..8c+7, input 8c + j in bits 4j..4j+3; with bits = 8 word c holds inputs 4c..4c+3,
+ *           input 4c + j in bits 8j..8j+7. Batched matrices (the experts) follow one another.
+ *   scales  [rows][in/64], biases [rows][in/64], fp16 or bf16 (scale_dtype): w = scales * q + biases.
+ * Read as bytes, a 4-bit word is the canonical int4 row (element 2c in the low nibble of byte c); 4-bit router
+ * and shared-expert tensors widen to the canonical int8 codes exactly, and bf16 scales and biases convert to fp16
+ * exactly in fp16's normal range. The shared expert's gate row (row E of the canonical router) comes
+ * unquantised and is quantised here to int8 group-64 affine: b = group min, s = (max - min) / 255 rounded to
+ * fp16, q = round((w - b) / s) clamped to 0..255. All pointers are host memory. */
+enum { MOE_DTYPE_F16 = 0, MOE_DTYPE_BF16 = 1 };
+
+typedef struct {
+  const uint32_t *q;
+  const uint16_t *scales, *biases;
+  int bits;   /* 4 or 8; the routed experts' tensors must be 4 */
+} moe_affine_tensor_t;
+
+typedef struct {
+  moe_affine_tensor_t router;                 /* [E][H] */
+  moe_affine_tensor_t exp_gate, exp_up;       /* [E][I][H] */
+  moe_affine_tensor_t exp_down;               /* [E][H][I] */
+  moe_affine_tensor_t sh_gate, sh_up;         /* [Is][H] */
+  moe_affine_tensor_t sh_down;                /* [H][Is] */
+  const uint16_t *shared_gate;                /* [H], scale_dtype */
+  const uint16_t *rms_gamma;                  /* [H] fp16, or NULL */
+  int scale_dtype;                            /* MOE_DTYPE_F16 or MOE_DTYPE_BF16 */
+} moe_affine_weights_t;
+
+/* Convert affine-layout weights into the canonical layout, in host buffers the library allocates: *out then
+ * points at them (rms_gamma at the caller's). Free them with moe_affine_free. Host work only: no device is
+ * touched. MOE_ERR_INVALID_ARG: a NULL pointer, bits other than 4 / 8 (4 for the routed experts), an unknown
+ * scale_dtype, a value that is not finite or overflows fp16, or host memory that cannot be allocated. */
+MOE_API int moe_affine_convert(const moe_block_config_t *cfg, const moe_affine_weights_t *src,
+                               moe_block_weights_t *out);
+MOE_API void moe_affine_free(moe_block_weights_t *w);
+
+/* moe_affine_convert + moe_block_load_weights (from host memory) + moe_affine_free. */
+MOE_API int moe_block_load_affine(moe_block_t *blk, const moe_affine_weights_t *src, void *stream);
+
 /* Create a handle for one block on the current CUDA device. Allocates the device weight store (repacked
  * layout) and all scratch for max_tokens, so forward never allocates. Refuses configurations it has no
  * kernel for with MOE_ERR_UNSUPPORTED. *out is set only on success. */

@@ -233,6 +233,16 @@ extern "C" void moe_block_destroy(moe_block_t* b) {
   delete b;
 }
 
+extern "C" int moe_block_load_affine(moe_block_t* b, const moe_affine_weights_t* src, void* stream) {
+  if (!b || !src) return MOE_ERR_INVALID_ARG;
+  moe_block_weights_t w;
+  const int st = moe_affine_convert(&b->cfg, src, &w);
+  if (st != MOE_OK) return st;
+  const int r = moe_block_load_weights(b, &w, 0, stream);
+  moe_affine_free(&w);
+  return r;
+}
+
 extern "C" int moe_block_load_weights(moe_block_t* b, const moe_block_weights_t* w, int on_device, void* stream) {
   if (!b || !w) return MOE_ERR_INVALID_ARG;
   const void* req[] = {w->router_q, w->router_s, w->router_b, w->exp_gate_q, w->exp_gate_s, w->exp_gate_b,

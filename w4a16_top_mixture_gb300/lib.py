@@ -24,7 +24,8 @@ EXPORTS = ["moe_block_create", "moe_block_load_weights", "moe_block_forward", "m
            "moe_last_cuda_error", "moe_block_debug_dequant", "moe_block_debug_last_routing",
            "moe_block_debug_set_wait", "moe_block_debug_set_trace", "moe_block_last_launch_count",
            "moe_router_topk_noalloc", "moe_debug_decode_plan", "moe_stack_create", "moe_stack_load_layer",
-           "moe_stack_forward", "moe_stack_get_status", "moe_stack_layer", "moe_stack_destroy"]
+           "moe_stack_forward", "moe_stack_get_status", "moe_stack_layer", "moe_stack_destroy",
+           "moe_affine_convert", "moe_affine_free", "moe_block_load_affine"]
 
 
 class MoeError(RuntimeError):
@@ -45,6 +46,68 @@ class Config(ctypes.Structure):
 
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class AffineTensor(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("bits", ctypes.c_int)]
+
+
+AFFINE_TENSORS = ["router", "exp_gate", "exp_up", "exp_down", "sh_gate", "sh_up", "sh_down"]
+
+
+class AffineWeights(ctypes.Structure):
+    _fields_ = [(n, AffineTensor) for n in AFFINE_TENSORS] + [
+        ("shared_gate", ctypes.c_void_p), ("rms_gamma", ctypes.c_void_p), ("scale_dtype", ctypes.c_int)]
+
+
+DTYPES = {"f16": 0, "bf16": 1}
+
+
+def _affine_struct(aff: dict):
+    """An AffineWeights struct over host numpy arrays: aff[name] = (q uint32, scales uint16, biases uint16, bits)
+    for every name of AFFINE_TENSORS, aff["shared_gate"] uint16, aff["rms_gamma"] uint16 or absent,
+    aff["scale_dtype"] "f16" or "bf16". Returns the struct and the arrays it points into."""
+    keep = []
+    A = AffineWeights()
+
+    def ptr(a, dtype):
+        a = np.ascontiguousarray(a).view(dtype)
+        keep.append(a)
+        return a.ctypes.data
+
+    for n in AFFINE_TENSORS:
+        q, s, b, bits = aff[n]
+        setattr(A, n, AffineTensor(ptr(q, np.uint32), ptr(s, np.uint16), ptr(b, np.uint16), int(bits)))
+    A.shared_gate = ptr(aff["shared_gate"], np.uint16)
+    A.rms_gamma = ptr(aff["rms_gamma"], np.uint16) if aff.get("rms_gamma") is not None else None
+    A.scale_dtype = DTYPES[aff["scale_dtype"]]
+    return A, keep
+
+
+def affine_convert(cfg, aff: dict):
+    """The library's conversion of affine-layout host arrays (see _affine_struct) into the canonical layout: a
+    dict of numpy arrays (codes uint8, fp16 pairs as float16), copied out of the library's buffers. Host only."""
+    lib = load_library()
+    A, keep = _affine_struct(aff)
+    c = Config(cfg.hidden, cfg.n_experts, cfg.top_k, cfg.expert_inter, cfg.shared_inter, 64, 1)
+    W = Weights()
+    _check(lib.moe_affine_convert(ctypes.byref(c), ctypes.byref(A), ctypes.byref(W)), "moe_affine_convert")
+    H, E, I, Is = cfg.hidden, cfg.n_experts, cfg.expert_inter, cfg.shared_inter
+    shapes = {"router": ((E + 1, H), (E + 1, H // 64)), "exp_gate": ((E, I, H // 2), (E, I, H // 64)),
+              "exp_up": ((E, I, H // 2), (E, I, H // 64)), "exp_down": ((E, H, I // 2), (E, H, I // 64)),
+              "sh_gate": ((Is, H), (Is, H // 64)), "sh_up": ((Is, H), (Is, H // 64)), "sh_down": ((H, Is), (H, Is // 64))}
+    out = {}
+    try:
+        for n, (qs, ss) in shapes.items():
+            out[n + "_q"] = np.ctypeslib.as_array(ctypes.cast(getattr(W, n + "_q"), ctypes.POINTER(ctypes.c_uint8)),
+                                                  shape=qs).copy()
+            for sfx in ("_s", "_b"):
+                a = np.ctypeslib.as_array(ctypes.cast(getattr(W, n + sfx), ctypes.POINTER(ctypes.c_uint16)), shape=ss)
+                out[n + sfx] = a.copy().view(np.float16)
+    finally:
+        lib.moe_affine_free(ctypes.byref(W))
+    return out
 
 
 _LIB = None
@@ -80,6 +143,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_router_topk_noalloc.argtypes = [vp, vp, vp, i, i, i, vp, i, vp, vp, vp, vp]
     lib.moe_debug_decode_plan.argtypes = [ctypes.POINTER(Config), i, i, i, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_stack_create.argtypes = [ctypes.POINTER(Config), i, ctypes.c_float, ctypes.POINTER(vp)]
+    lib.moe_affine_convert.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(AffineWeights), ctypes.POINTER(Weights)]
+    lib.moe_affine_free.argtypes = [ctypes.POINTER(Weights)]
+    lib.moe_affine_free.restype = None
+    lib.moe_block_load_affine.argtypes = [vp, ctypes.POINTER(AffineWeights), vp]
     lib.moe_stack_load_layer.argtypes = [vp, i, ctypes.POINTER(Weights), i, vp]
     lib.moe_stack_forward.argtypes = [vp, vp, vp, i, vp, vp]
     lib.moe_stack_get_status.argtypes = [vp, ctypes.POINTER(u32)]
@@ -170,6 +237,12 @@ class MoeBlock:
         W, keep, on_dev = _weights_struct(w)
         _check(self.lib.moe_block_load_weights(self.handle, ctypes.byref(W), int(on_dev), _stream_ptr(stream)),
                "moe_block_load_weights")
+
+    def load_affine(self, aff: dict, stream=None):
+        """aff: host arrays in the affine checkpoint layout (see _affine_struct)."""
+        A, keep = _affine_struct(aff)
+        _check(self.lib.moe_block_load_affine(self.handle, ctypes.byref(A), _stream_ptr(stream)),
+               "moe_block_load_affine")
 
     def forward(self, x, out=None, stream=None):
         import torch
