@@ -135,6 +135,28 @@ def test_chunk_split_is_byte_equal():
     blk.close()
 
 
+@pytest.mark.parametrize("T", [517, 600])
+def test_chunk_repeats_are_byte_equal(T):
+    """The same chunk forwarded again and again on one handle gives the same bytes every time: the GEMM's
+    handoffs leave no room for timing to change a result. (When two threads of a CTA issued the MMAs, about one
+    forward in thirty at these sizes had one job computed wrongly; 24 repeats of two shapes would have shown it
+    with high probability.)"""
+    import torch
+    build.build()
+    cfg = synth.PROD
+    w, x = make_case(cfg, T, 80)
+    blk = lib.MoeBlock.from_config(cfg, max_tokens=T)
+    blk.load_weights(lib.upload_weights(w))
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
+    first = blk.forward(xd).cpu().numpy().view(np.uint16).copy()
+    for rep in range(23):
+        again = blk.forward(xd).cpu().numpy().view(np.uint16)
+        bad = np.nonzero((again != first).any(axis=1))[0]
+        assert len(bad) == 0, (rep, bad[:16].tolist())
+    assert blk.status()[0] == 0
+    blk.close()
+
+
 def test_chunk_bounded_wait_reports_timeout_and_recovers():
     """A withheld weight copy (host-set test flag) makes one CTA's bounded waits of the chunk GEMM run out: the
     call ends, the status reports the timeout, and the next call on the same handle is correct again. No GPU

@@ -9,11 +9,16 @@
 //
 // Persistent CTAs (one per SM) take jobs j = blockIdx.x + k * gridDim.x. Warp roles, all stepping through the
 // same jobs and K-tiles and handing stages over on mbarriers:
-//   warps 0, 15  producers of the even (warp 0) or odd (warp 15) K-tiles: a bulk copy of the K-tile's weight
+//   warps 0, 14  producers of the even (warp 0) or odd (warp 14) K-tiles: a bulk copy of the K-tile's weight
 //              block (codes + pairs), TMA tensor loads of the activation rows (128-byte swizzled K-major) and a
 //              bulk copy of the rows' sums over the K-tile's 64 columns, all on the stage's "full" barrier
-//   warps 1, 14  lane 0 issues the MMAs of the even (warp 1) or odd (warp 14) K-tiles (A from tensor memory,
-//              B from shared memory) and commits them to the stage's "empty" barrier; warp 1 also owns TMEM
+//   warp 1     the MMAs of every K-tile (A from tensor memory, B from shared memory), committed to the stage's
+//              "empty" barrier; it also owns TMEM. One thread issues all of the CTA's MMAs and commits: with two
+//              issuing threads (alternate K-tiles), about one forward in thirty at 512 tokens came out with a
+//              job at the start of a CTA's work corrupted.
+// The producer and MMA warps step through their loops as whole warps, so that every copy and MMA operand is
+// warp-uniform, and one elected lane issues the copies or the MMAs: with the loop in one lane, each issue cost
+// that lane several hundred cycles (the MMAs of a K-tile: ~530 traced cycles, now ~75).
 //   warps 2-9  dequantise, two groups of four warps taking alternate K-tiles: thread = band row = TMEM lane,
 //              codes -> exact fp16 integers stored straight into the slot's A columns of tensor memory
 //   warps 10-13 fold (thread = TMEM lane = band row) and, after the job's last K-tile, the epilogue
@@ -44,7 +49,7 @@ namespace {
 
 enum : int { GK_ROUTER = 0, GK_SHGU = 1, GK_SHDN = 2, GK_EXGU = 3, GK_EXDN = 4 };
 
-constexpr int GTH = 512;                // 16 warps
+constexpr int GTH = 480;                // 15 warps
 constexpr int NSG_MAX = 16;             // shared-memory stages (the count depends on the phase, see Geo)
 constexpr int NT_MAX = 8;               // tensor-memory slots (the count depends on the widest tile, see Slots)
 // The stages share one area. A stage is weight block | B hi (up to 64 rows x 128 B, swizzled) | [B lo], each
@@ -258,12 +263,11 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   const int nt = min(NT_MAX, (int)(512 / slot_cols));
   float* sums = reinterpret_cast<float*>(smem + S_SUMS);   // [NSG_MAX][SUM_RUN]
 
-  if (warp == 0 || warp == 15) {
+  if (warp == 0 || warp == 14) {
     // ------------------------------------------------------------------ producers
-    // Warp 0 fills the stages of the even K-tiles, warp 15 those of the odd ones: issuing a copy costs its
-    // thread about a hundred cycles, too slow for one thread to keep up. The warp steps through the loop
-    // together; lane 0 arms the stage, and lanes 0 and 1 issue their copies in one instruction each: the
-    // weight block and the sums run (1-D bulk copies), then B hi and B lo (tensor loads).
+    // Warp 0 fills the stages of the even K-tiles, warp 14 those of the odd ones. The whole warp steps through
+    // the loop, so every copy operand is warp-uniform, and one elected lane arms the stage and issues its
+    // copies: the weight block and the sums run (1-D bulk copies), then B hi and B lo (tensor loads).
     const uint32_t par = warp == 0 ? 0u : 1u;
     uint32_t gk = 0;
     bool run = true;
@@ -279,14 +283,11 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       const int box = jb.n <= 16 ? 0 : jb.n <= 32 ? 1 : 2;
       const bool lo = jb.lomap >= 0;
       const uint32_t tx = (uint32_t)(blk + SUMS_BYTES) + (16u << box) * 128u * (lo ? 2u : 1u);
-      // lane 0: the weight block and B hi; lane 1: the K-tile's sums for the tile's rows (SUM_RUN floats from
-      // the first row rounded down to a multiple of 4: 16-byte aligned, the row strides being multiples of 4
-      // floats) and B lo
-      const uint8_t* bsrc = lane == 0 ? jb.w : reinterpret_cast<const uint8_t*>(jb.sum + (jb.row0 & ~3));
-      const size_t bstep = lane == 0 ? (size_t)blk : (size_t)jb.sstride * 4;
-      const uint32_t bbytes = lane == 0 ? (uint32_t)blk : (uint32_t)SUMS_BYTES;
-      const CUtensorMap* map = &g.maps.m[lane == 1 && lo ? jb.lomap : jb.bmap][box];
-      const bool tload = lane == 0 || (lane == 1 && lo);
+      // the K-tile's sums for the tile's rows: SUM_RUN floats from the first row rounded down to a multiple of
+      // 4 (16-byte aligned, the row strides being multiples of 4 floats)
+      const float* srun = jb.sum + (jb.row0 & ~3);
+      const CUtensorMap* mhi = &g.maps.m[jb.bmap][box];
+      const CUtensorMap* mlo = &g.maps.m[lo ? jb.lomap : jb.bmap][box];
       for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sr.next(NSG)) {
         if ((gk & 1u) != par) continue;
         const int s = sr.t;
@@ -294,13 +295,15 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
         if (withhold && gk == 0) continue;
         uint8_t* st = smem + s * geo.bytes;
-        if (lane == 0) mbar_expect_tx(&bar->full[s], tx);
+        if (elect_one()) {
+          mbar_expect_tx(&bar->full[s], tx);
+          bulk_g2s(st + ST_W, jb.w + (size_t)kt * blk, (uint32_t)blk, &bar->full[s]);
+          bulk_g2s(sums + s * SUM_RUN, srun + (size_t)kt * jb.sstride, (uint32_t)SUMS_BYTES, &bar->full[s]);
+          tma_load_2d(st + geo.bhi, mhi, kt * 64, jb.row0, &bar->full[s]);
+          if (lo) tma_load_2d(st + geo.blo, mlo, kt * 64, jb.row0, &bar->full[s]);
+          GSTAMP(0, gk);
+        }
         __syncwarp();
-        if (lane < 2)
-          bulk_g2s(lane == 0 ? st + ST_W : reinterpret_cast<uint8_t*>(sums + s * SUM_RUN), bsrc + kt * bstep,
-                   bbytes, &bar->full[s]);
-        if (tload) tma_load_2d(st + (lane == 0 ? geo.bhi : geo.blo), map, kt * 64, jb.row0, &bar->full[s]);
-        if (lane == 0) GSTAMP(0, gk);
       }
     }
     // drain: every copy this warp issued must have landed before the CTA leaves (the withheld one was never
@@ -311,33 +314,32 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         if ((q & 1u) == par && !(withhold && q == 0)) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
     }
     __syncwarp();
-  } else if (warp == 1 || warp == 14) {
-    // ------------------------------------------------------------------ MMA issue (lane 0)
-    // Two issuing threads, alternate K-tiles: one thread's tcgen05.mma issue costs tens of cycles, and the
-    // accumulators of consecutive K-tiles are independent.
-    const uint32_t par = warp == 1 ? 0u : 1u;
-    if (lane == 0) {
-      uint32_t gk = 0;
-      bool run = true;
-      JobIter it;
-      job_begin(g, ngroups, tw, it);
-      Job jb;
-      SlotRing sl, sr;
-      while (run && job_next(g, it, jb)) {
-        const uint32_t idesc = umma_idesc_f16(128, jb.n);
-        const bool lo = jb.lomap >= 0;
-        for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
-          if ((gk & 1u) != par) continue;
-          const int s = sr.t, t = sl.t;
-          // a_ready implies full[s] and that the fold of K-tile gk - nt released slot t (the dequantisation
-          // waited for both)
-          if (!wait(&bar->a_ready[t], sl.ph)) { run = false; break; }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issue
+    // The whole warp steps through the loop and waits, so the descriptors and TMEM addresses are warp-uniform;
+    // one elected lane (the same one every time) issues the MMAs and the commit.
+    uint32_t gk = 0;
+    bool run = true;
+    JobIter it;
+    job_begin(g, ngroups, tw, it);
+    Job jb;
+    SlotRing sl, sr;
+    while (run && job_next(g, it, jb)) {
+      const uint32_t idesc = umma_idesc_f16(128, jb.n);
+      const bool lo = jb.lomap >= 0;
+      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
+        const int s = sr.t, t = sl.t;
+        // a_ready implies full[s] and that the fold of K-tile gk - nt released slot t (the dequantisation
+        // waited for both)
+        const bool ok = wait(&bar->a_ready[t], sl.ph);
+        if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
+        tc_fence_after();
+        // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
+        const uint8_t* st = smem + s * geo.bytes;
+        const uint64_t bh = umma_desc_sw128(smem_u32(st + geo.bhi)), bl = umma_desc_sw128(smem_u32(st + geo.blo));
+        const uint32_t d = tmem + t * slot_cols, a = d + a_col;
+        if (elect_one()) {
           GSTAMP(6, gk);
-          tc_fence_after();
-          // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
-          const uint8_t* st = smem + s * geo.bytes;
-          const uint64_t bh = umma_desc_sw128(smem_u32(st + geo.bhi)), bl = umma_desc_sw128(smem_u32(st + geo.blo));
-          const uint32_t d = tmem + t * slot_cols, a = d + a_col;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, ks > 0 ? 1u : 0u);
           if (lo)
@@ -346,11 +348,11 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
           umma_commit(&bar->empty[s]);
           GSTAMP(3, gk);
         }
+        __syncwarp();
       }
-      // this thread's last MMAs must have completed before TMEM is released
-      const uint32_t last = gk == 0 ? 0u : ((gk - 1) & 1u) == par ? gk - 1 : gk - 2;
-      if (gk > par) mbar_wait(&bar->empty[last % NSG], (last / NSG) & 1u, to);
     }
+    // the last MMAs must have completed before TMEM is released (a commit tracks all earlier MMAs of its thread)
+    if (lane == 0 && gk > 0) mbar_wait(&bar->empty[(gk - 1) % NSG], ((gk - 1) / NSG) & 1u, to);
     __syncwarp();
   } else if (warp < 10) {
     // ------------------------------------------------------------------ dequantise
