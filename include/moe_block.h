@@ -126,7 +126,10 @@ MOE_API int moe_block_create(const moe_block_config_t *cfg, moe_block_t **out);
 
 /* Copy and repack the canonical weights into the handle. weights_on_device = 1: the pointers are device
  * memory; 0: host memory (copied through a temporary device buffer). The caller keeps ownership and may free
- * its buffers once this returns (the call synchronises `stream`). */
+ * its buffers once this returns (the call synchronises `stream`). A handle that serves prompt chunks
+ * (max_tokens > 16) forms s * q in fp16 (as an exact pair of halves) on its chunk path, so it refuses with
+ * MOE_ERR_INVALID_ARG, and stays unloaded, when a scale is not finite or |s| * (largest code: 15 for int4, 255
+ * for int8) reaches 65504; decode-only handles compute in fp32 and have no such limit. */
 MOE_API int moe_block_load_weights(moe_block_t *blk, const moe_block_weights_t *w, int weights_on_device, void *stream);
 
 /* out[T][H] = block(x[T][H]). x and out are caller-owned device buffers of fp16, 16-byte aligned, not

@@ -151,3 +151,22 @@ def test_nonfinite_activations_keep_routing_in_bounds(cfgname, T):
     _valid_routing(ids2, cfg.n_experts, cfg.top_k)
     if good.size:
         np.testing.assert_array_equal(ids2[good], r["ids"])
+
+
+@pytest.mark.parametrize("name,value", [("exp_down_s", 5000.0), ("sh_up_s", 300.0)])
+def test_chunk_handle_refuses_out_of_range_scale(name, value):
+    """A handle that serves prompt chunks forms s * q in fp16 on its chunk path: it refuses scales whose product
+    with the largest code (15 for int4, 255 for int8) reaches 65504, and stays unloaded. A decode-only handle
+    (max_tokens <= 16, fp32 arithmetic) takes the same weights."""
+    cfg = synth.TINY
+    w = synth.gen_layer(cfg, 5)
+    w[name] = w[name].copy()
+    w[name].flat[3] = np.float16(value)
+    chunky = lib.MoeBlock.from_config(cfg, max_tokens=40)
+    with pytest.raises(lib.MoeError) as e:
+        chunky.load_weights(w)
+    assert e.value.status == -1
+    chunky.close()
+    dec = lib.MoeBlock.from_config(cfg, max_tokens=16)
+    dec.load_weights(w)
+    dec.close()

@@ -288,7 +288,9 @@ extern "C" int moe_block_load_weights(moe_block_t* b, const moe_block_weights_t*
   src.sh_down_q = (const uint8_t*)dptr[18]; src.sh_down_s = (const uint16_t*)dptr[19]; src.sh_down_b = (const uint16_t*)dptr[20];
   RepackDst dst{b->router, b->sh_gu, b->sh_dn, b->ex_gu, b->ex_dn};
   cudaError_t e = repack_all(src, b->L, dst, st);
-  if (e == cudaSuccess && b->chunk) e = gemm_repack(src, b->G, st);
+  // the repack's scale-range flag: a spare word of the chunk scratch's control block
+  uint32_t* range_bad = b->chunk ? reinterpret_cast<uint32_t*>(b->CS.ctl) + 8 : nullptr;
+  if (e == cudaSuccess && b->chunk) e = gemm_repack(src, b->G, range_bad, st);
   if (e == cudaSuccess && w->rms_gamma) {
     e = cudaMemcpyAsync(b->gamma, w->rms_gamma, H * 2, on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
                         st);
@@ -296,6 +298,15 @@ extern "C" int moe_block_load_weights(moe_block_t* b, const moe_block_weights_t*
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (tmp) cudaFree(tmp);
   if (e != cudaSuccess) return cuda_fail(e, "moe_block_load_weights");
+  if (b->chunk) {
+    uint32_t bad = 0;
+    e = cudaMemcpy(&bad, range_bad, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_block_load_weights");
+    if (bad) {
+      b->loaded = false;
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
   b->has_gamma = w->rms_gamma != nullptr;
   b->loaded = true;
   return MOE_OK;

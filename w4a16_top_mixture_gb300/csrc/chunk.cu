@@ -42,11 +42,13 @@ GemmLayout gemm_layout_carve(const MoeLayout& L, uint8_t* base) {
 
 // One thread per (batch, row, K-tile): copies the row's 64 codes of that tile (32 or 64 bytes) and its (s, b)
 // pair into the tile block. rowmode 0 keeps the row index; 1 / 2 place row r of a gate / up matrix into band
-// r/64 at position (0 | 64) + r%64. int8 rows get the P8 byte order inside each 8-byte block.
+// r/64 at position (0 | 64) + r%64. int8 rows get the P8 byte order inside each 8-byte block. The GEMM forms
+// s * q in fp16 (as an exact pair of halves), so a scale that is not finite, or whose product with the largest
+// code reaches fp16's largest finite value, sets *range_bad.
 __global__ void k_gemm_tiles(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s,
                              const uint16_t* __restrict__ b, int nbatch, int nrows, int cols, int int8,
                              size_t src_q_batch, size_t src_sb_batch, uint8_t* __restrict__ dst,
-                             size_t dst_batch, int rowmode) {
+                             size_t dst_batch, int rowmode, uint32_t* __restrict__ range_bad) {
   const int KT = cols / 64, cb = int8 ? 64 : 32, blk = int8 ? GEMM_BLK8 : GEMM_BLK4;
   const int rowbytes = int8 ? cols : cols / 2;
   const size_t n = (size_t)nbatch * nrows * KT;
@@ -71,6 +73,8 @@ __global__ void k_gemm_tiles(const uint8_t* __restrict__ q, const uint16_t* __re
     }
     const size_t si = bt * src_sb_batch + (size_t)r * KT + kt;
     *reinterpret_cast<uint32_t*>(tile + 128 * cb + rr * 4) = (uint32_t)s[si] | ((uint32_t)b[si] << 16);
+    const float sv = __half2float(__ushort_as_half(s[si]));
+    if (!(fabsf(sv) * (int8 ? 255.0f : 15.0f) < 65504.0f)) atomicOr(range_bad, 1u);
   }
 }
 
@@ -80,15 +84,17 @@ static int grid_for_n(size_t n) {
   return g < 1 ? 1 : (int)g;
 }
 
-cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, cudaStream_t st) {
+cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, uint32_t* range_bad, cudaStream_t st) {
   const int H = G.H, E = G.E, I = G.I, Is = G.Is;
   // the router's padding rows stay zero: codes 0, s = b = 0
   cudaError_t e = cudaMemsetAsync(G.gr, 0, (size_t)(G.Mr / 128) * (H / 64) * GEMM_BLK8, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(range_bad, 0, 4, st);
   if (e != cudaSuccess) return e;
   auto tiles = [&](const uint8_t* q, const uint16_t* s, const uint16_t* b, int nbatch, int nrows, int cols,
                    int int8, size_t sqb, size_t ssb, uint8_t* dst, size_t db, int rowmode) {
     const size_t n = (size_t)nbatch * nrows * (cols / 64);
-    k_gemm_tiles<<<grid_for_n(n), 256, 0, st>>>(q, s, b, nbatch, nrows, cols, int8, sqb, ssb, dst, db, rowmode);
+    k_gemm_tiles<<<grid_for_n(n), 256, 0, st>>>(q, s, b, nbatch, nrows, cols, int8, sqb, ssb, dst, db, rowmode,
+                                                 range_bad);
   };
   tiles(w.router_q, w.router_s, w.router_b, 1, E + 1, H, 1, 0, 0, G.gr, 0, 0);
   tiles(w.sh_gate_q, w.sh_gate_s, w.sh_gate_b, 1, Is, H, 1, 0, 0, G.gsgu, 0, 1);

@@ -45,7 +45,9 @@ struct GemmLayout {
 size_t gemm_store_bytes(const MoeLayout& L);
 // carve a GEMM layout out of `base` (gemm_store_bytes bytes, 256-byte aligned)
 GemmLayout gemm_layout_carve(const MoeLayout& L, uint8_t* base);
-cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, cudaStream_t st);
+// repack into the GEMM layout; *range_bad (a device word) ends up nonzero when a scale is out of the GEMM's range
+// (see k_gemm_tiles)
+cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, uint32_t* range_bad, cudaStream_t st);
 
 constexpr int CHUNK_NT = 64;   // tokens (rows of activations) per GEMM tile
 
@@ -72,7 +74,8 @@ struct ChunkScratch {
   uint16_t* hh_lo;     // [Tm*K][I] fp16 P8, routed h (low half, scaled by 4096)
   float* y;            // [Tm*K][H] routed expert outputs (unweighted)
   int4* groups;        // [E + Tm*K/CHUNK_NT + 1] (expert, first sorted row, rows) per row tile
-  int32_t* ctl;        // [16] ctl[0] row-tile count, ctl[1] rows of the widest row tile
+  int32_t* ctl;        // [16] ctl[0] row-tile count, ctl[1] rows of the widest row tile; ctl[8] the weight
+                       // repack's scale-range flag
   float* sum_xp;       // [H/64][sp]   sums of xp's rows
   float* sum_xs;       // [H/64][sr]   sums of xs's rows
   float* sum_hs;       // [Is/64][sp]  sums of hs + hs_lo / 4096

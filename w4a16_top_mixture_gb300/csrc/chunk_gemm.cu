@@ -184,6 +184,7 @@ __device__ __forceinline__ bool job_next(const GemmArgs& g, JobIter& it, Job& jb
 
 struct Bars {
   uint64_t full[NSG_MAX], empty[NSG_MAX], a_ready[NT_MAX], d_free[NT_MAX];
+  uint64_t acc_full[2], acc_free[2];   // a job's accumulator (job parity) is complete / has been read
   uint64_t fold_sync;   // the four fold warps meet here in the SwiGLU epilogue (a bounded wait)
   uint32_t tslot;
   int ngroups, tw;      // the launch's row-tile count and token-tile width, read once
@@ -240,6 +241,10 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       mbar_init(&bar->d_free[i], 4);
     }
     mbar_init(&bar->fold_sync, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar->acc_full[b], 1);   // the MMA issuer's commit after the job's last K-tile
+      mbar_init(&bar->acc_free[b], 4);   // the fold warps, once they have read the accumulator
+    }
     bar->abort = 0;
     // phase 1 tiles the tokens 64 at a time; phases 2 and 3 take the bucketing's row tiles, and phase 3 tiles
     // the shared down's tokens as wide as the widest row tile, so no job is wider than that
@@ -255,12 +260,13 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   const Geo geo = geo_of(g.phase);
   const uint32_t NSG = (uint32_t)geo.nsg;
   const int ngroups = bar->ngroups, tw = bar->tw;
-  // slot geometry: accumulator hi (aw columns) | [phase 3: accumulator lo (aw)] | A: 128 rows x 64 fp16 (32
-  // columns), aw = the widest job's N rounded up to 32 columns; as many slots as fit the 512 columns
+  // tensor memory: two job accumulators (job parity), each aw columns (aw = the widest job's N rounded up to
+  // 32) plus, in phase 3, a low-half accumulator of aw more; then the A slots, 64 columns each: A1 = fp16(s q)
+  // and A2 = s q - A1 (exact), 128 rows x 64 K each
   const bool lo_phase = g.phase == 3;
   const uint32_t aw = (uint32_t)((min(tw, g.phase == 1 ? ((min(g.T, CHUNK_NT) + 15) & ~15) : CHUNK_NT) + 31) & ~31);
-  const uint32_t tlo = aw, a_col = lo_phase ? 2 * aw : aw, slot_cols = a_col + 32;
-  const int nt = min(NT_MAX, (int)(512 / slot_cols));
+  const uint32_t dcols = lo_phase ? 2 * aw : aw, tlo = aw, a0 = 2 * dcols;
+  const int nt = min(NT_MAX, (int)((512 - a0) / 64));
   float* sums = reinterpret_cast<float*>(smem + S_SUMS);   // [NSG_MAX][SUM_RUN]
 
   if (warp == 0 || warp == 14) {
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     // ------------------------------------------------------------------ MMA issue
     // The whole warp steps through the loop and waits, so the descriptors and TMEM addresses are warp-uniform;
     // one elected lane (the same one every time) issues the MMAs and the commit.
-    uint32_t gk = 0;
+    uint32_t gk = 0, njob = 0;
     bool run = true;
     JobIter it;
     job_begin(g, ngroups, tw, it);
@@ -327,6 +333,12 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     while (run && job_next(g, it, jb)) {
       const uint32_t idesc = umma_idesc_f16(128, jb.n);
       const bool lo = jb.lomap >= 0;
+      const uint32_t b = njob & 1u, d = tmem + b * dcols;
+      // the job accumulates in accumulator b, which the fold of job njob - 2 must have read
+      {
+        const bool ok = njob < 2 || wait(&bar->acc_free[b], ((njob >> 1) - 1) & 1u);
+        if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
+      }
       for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
         const int s = sr.t, t = sl.t;
         // a_ready implies full[s] and that the fold of K-tile gk - nt released slot t (the dequantisation
@@ -337,19 +349,27 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
         const uint8_t* st = smem + s * geo.bytes;
         const uint64_t bh = umma_desc_sw128(smem_u32(st + geo.bhi)), bl = umma_desc_sw128(smem_u32(st + geo.blo));
-        const uint32_t d = tmem + t * slot_cols, a = d + a_col;
+        const uint32_t a = tmem + a0 + 64u * (uint32_t)t;
         if (elect_one()) {
           GSTAMP(6, gk);
+          // D += A1 B + A2 B: the exact products s q x, summed over the whole job
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < 4; ++ks) {
+            umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
+            umma_f16_ts(d, a + 32 + 8 * ks, bh + 2 * ks, idesc, 1u);
+          }
+          // the low halves of the activations: A2's share there is below fp32 resolution of the sum
           if (lo)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) umma_f16_ts(d + tlo, a + 8 * ks, bl + 2 * ks, idesc, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+              umma_f16_ts(d + tlo, a + 8 * ks, bl + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&bar->empty[s]);
+          if (kt == jb.ktiles - 1) umma_commit(&bar->acc_full[b]);
           GSTAMP(3, gk);
         }
         __syncwarp();
       }
+      ++njob;
     }
     // the last MMAs must have completed before TMEM is released (a commit tracks all earlier MMAs of its thread)
     if (lane == 0 && gk > 0) mbar_wait(&bar->empty[(gk - 1) % NSG], ((gk - 1) / NSG) & 1u, to);
@@ -382,42 +402,54 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         // row r's (s, b) pair and the sums of the tile's activation rows
         {
           uint32_t* side = reinterpret_cast<uint32_t*>(smem + S_SIDE + t * SIDE_BYTES);
-          side[r] = *reinterpret_cast<const uint32_t*>(st + 128 * (jb.int8 ? 64 : 32) + r * 4);
+          side[r] = *reinterpret_cast<const uint32_t*>(st + 128 * (jb.int8 ? 64 : 32) + r * 4);   // (s, b)
           if (r < CHUNK_NT) reinterpret_cast<float*>(side)[128 + r] = sums[s * SUM_RUN + (jb.row0 & 3) + r];
         }
-        // row r of A in K order: column 4c + k of the slot holds the fp16 pair k of 8-column block c
-        uint32_t arow[32];
-        if (jb.int8) {
-          const uint8_t* codes = st + r * 64;
+        // row r of A1 and A2 in K order: column 4c + k holds the pair k of 8-column block c, A1 = fp16(s q),
+        // A2 = s q - A1 (exact: s q is a multiple of s's unit in the last place with at most 19 significant bits,
+        // so the rounding residual has at most 9 and is a multiple of that unit, never below 2^-24). Two halves of
+        // 16 columns each, stored as soon as they are made.
+        const uint32_t sbw = *reinterpret_cast<const uint32_t*>(st + 128 * (jb.int8 ? 64 : 32) + r * 4);
+        const __half2 s2 = __low2half2(*reinterpret_cast<const __half2*>(&sbw));
+        const uint32_t ta = trow + a0 + 64u * (uint32_t)t;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint2 w = *reinterpret_cast<const uint2*>(codes + c * 8);
-            uint32_t v[4];
-            int8_block_pairs(w.x, w.y, v);
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          uint32_t a1[16], a2[16];
+          auto put = [&](int i, __half2 q) {
+            const __half2 h1 = __hmul2(q, s2);
+            const __half2 h2 = __hfma2(q, s2, __hneg2(h1));
+            a1[i] = *reinterpret_cast<const uint32_t*>(&h1);
+            a2[i] = *reinterpret_cast<const uint32_t*>(&h2);
+          };
+          if (jb.int8) {
+            const uint8_t* codes = st + r * 64 + hlf * 32;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&v[k]), k1024);
-              arow[4 * c + k] = *reinterpret_cast<const uint32_t*>(&q);
+            for (int c = 0; c < 4; ++c) {
+              const uint2 w = *reinterpret_cast<const uint2*>(codes + c * 8);
+              uint32_t v[4];
+              int8_block_pairs(w.x, w.y, v);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) put(4 * c + k, __hsub2(*reinterpret_cast<const __half2*>(&v[k]), k1024));
+            }
+          } else {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(st + r * 32 + hlf * 16);
+            const uint32_t wd[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t v[4];
+              int4_word_pairs(wd[c], v);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const __half2 h = *reinterpret_cast<const __half2*>(&v[k]);
+                // exact codes: 1024 + q -> q; 1024 + 16 q (odd pairs) -> q
+                put(4 * c + k, (k & 1) ? __hfma2(h, k16, k64) : __hsub2(h, k1024));
+              }
             }
           }
-        } else {
-          const uint8_t* codes = st + r * 32;
-          const uint4 w0 = *reinterpret_cast<const uint4*>(codes), w1 = *reinterpret_cast<const uint4*>(codes + 16);
-          const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t v[4];
-            int4_word_pairs(wd[c], v);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const __half2 h = *reinterpret_cast<const __half2*>(&v[k]);
-              // exact codes: 1024 + q -> q; 1024 + 16 q (odd pairs) -> q
-              const __half2 q = (k & 1) ? __hfma2(h, k16, k64) : __hsub2(h, k1024);
-              arow[4 * c + k] = *reinterpret_cast<const uint32_t*>(&q);
-            }
-          }
+          tmem_st16(ta + 16u * hlf, a1);
+          tmem_st16(ta + 32u + 16u * hlf, a2);
         }
-        tmem_st32(trow + t * slot_cols + a_col, arow);
+        tmem_wait_st();
         tc_fence_before();   // the MMAs read A after the a_ready handoff
         __syncwarp();
         if (lane == 0) {
@@ -435,7 +467,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     float* ep = reinterpret_cast<float*>(smem + S_EP);      // [128 rows][65] the job's accumulator
     const GemmLayout& G = g.G;
     const ChunkScratch& S = g.S;
-    uint32_t fph = 0;
+    uint32_t fph = 0, njob = 0;
     // the four fold warps meet (bounded: a warp that has aborted makes the others time out, never hang)
     auto fold_sync = [&]() -> bool {
       __syncwarp();
@@ -467,27 +499,17 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         const uint32_t* side = reinterpret_cast<const uint32_t*>(smem + S_SIDE + t * SIDE_BYTES);
         const float2 sb = h2f(side[r]);
         const float4* xs4 = reinterpret_cast<const float4*>(side + 128);
-        const uint32_t d = trow + t * slot_cols;
-        const float slo = sb.x * (1.0f / 4096.0f);
-        // 16 columns at a time; the low-half accumulator after the high one, so that one 16-register buffer
-        // serves both (the 64 accumulators stay in registers)
+        // the affine's offset part of the group: acc += b * sum(x) (the scaled codes accumulate in TMEM)
 #pragma unroll
         for (int c0 = 0; c0 < CHUNK_NT; c0 += 16) {
           if (c0 < jb.n) {
-            uint32_t v[16];
-            tmem_ld16_nowait(d + c0, v);
-            tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 16; i += 4) {
               const float4 x4 = xs4[(c0 + i) >> 2];
-              const float xv = (i & 3) == 0 ? x4.x : (i & 3) == 1 ? x4.y : (i & 3) == 2 ? x4.z : x4.w;
-              acc[c0 + i] = fmaf(sb.x, __uint_as_float(v[i]), fmaf(sb.y, xv, acc[c0 + i]));
-            }
-            if (jb.lomap >= 0) {
-              tmem_ld16_nowait(d + tlo + c0, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(slo, __uint_as_float(v[i]), acc[c0 + i]);
+              acc[c0 + i] = fmaf(sb.y, x4.x, acc[c0 + i]);
+              acc[c0 + i + 1] = fmaf(sb.y, x4.y, acc[c0 + i + 1]);
+              acc[c0 + i + 2] = fmaf(sb.y, x4.z, acc[c0 + i + 2]);
+              acc[c0 + i + 3] = fmaf(sb.y, x4.w, acc[c0 + i + 3]);
             }
           }
         }
@@ -497,6 +519,33 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         if (r == 0) GSTAMP(5, gk);
       }
       if (!run) break;
+      // ---- the job's accumulator: s * sum(q x) over all its K-tiles (+ the low halves' share / 4096)
+      {
+        const uint32_t b = njob & 1u;
+        if (!wait(&bar->acc_full[b], (njob >> 1) & 1u)) break;
+        tc_fence_after();
+        const uint32_t d = trow + b * dcols;
+#pragma unroll
+        for (int c0 = 0; c0 < CHUNK_NT; c0 += 16) {
+          if (c0 < jb.n) {
+            uint32_t v[16];
+            tmem_ld16_nowait(d + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[c0 + i] += __uint_as_float(v[i]);
+            if (jb.lomap >= 0) {
+              tmem_ld16_nowait(d + tlo + c0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(__uint_as_float(v[i]), 1.0f / 4096.0f, acc[c0 + i]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->acc_free[b]);
+        ++njob;
+      }
       // ---- epilogue. The accumulator goes to shared memory (its register indices are compile-time, so this
       // is the only unrolled step), then short loops over the tile's tokens write the results: the code that
       // runs once per job stays small.
