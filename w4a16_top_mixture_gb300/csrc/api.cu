@@ -209,6 +209,8 @@ extern "C" int moe_block_create(const moe_block_config_t* cfg, moe_block_t** out
     b->chunk = true;
     e = cudaMalloc(&b->gstore, gemm_store_bytes(L));
     if (e == cudaSuccess) e = cudaMalloc(&b->cscratch, chunk_scratch_bytes(L, c.max_tokens));
+    // zero once: the group-sum rows' entries past the matrices' groups stay zero (the GEMM multiplies them)
+    if (e == cudaSuccess) e = cudaMemset(b->cscratch, 0, chunk_scratch_bytes(L, c.max_tokens));
     if (e == cudaSuccess) {
       b->G = gemm_layout_carve(L, b->gstore);
       b->CS = chunk_scratch_carve(L, c.max_tokens, b->cscratch);

@@ -119,9 +119,7 @@ size_t chunk_scratch_bytes(const MoeLayout& L, int Tm) {
   b += al256(TK * H * 2);
   b += al256(TK * I * 2) * 2 + al256(TK * H * 4);
   b += al256((E + TK / CHUNK_NT + 2) * 16) + al256(16 * 4);
-  const size_t sp = (T + 3) & ~(size_t)3, sr = (TK + 3) & ~(size_t)3;
-  b += al256(((H / 64) * sp + SUM_SLACK) * 4) + al256(((H / 64) * sr + SUM_SLACK) * 4);
-  b += al256(((Is / 64) * sp + SUM_SLACK) * 4) + al256(((I / 64) * sr + SUM_SLACK) * 4);
+  b += al256(T * GSUM_COLS * 2) * 2 + al256(TK * GSUM_COLS * 2) * 2;
   return b;
 }
 
@@ -148,13 +146,10 @@ ChunkScratch chunk_scratch_carve(const MoeLayout& L, int Tm, uint8_t* base) {
   S.y = (float*)take(TK * H * 4);
   S.groups = (int4*)take((E + TK / CHUNK_NT + 2) * 16);
   S.ctl = (int32_t*)take(16 * 4);
-  const size_t sp = (T + 3) & ~(size_t)3, sr = (TK + 3) & ~(size_t)3;
-  S.sp = (int)sp;
-  S.sr = (int)sr;
-  S.sum_xp = (float*)take(((H / 64) * sp + SUM_SLACK) * 4);
-  S.sum_xs = (float*)take(((H / 64) * sr + SUM_SLACK) * 4);
-  S.sum_hs = (float*)take(((Is / 64) * sp + SUM_SLACK) * 4);
-  S.sum_hh = (float*)take(((I / 64) * sr + SUM_SLACK) * 4);
+  S.gs_xp = (uint16_t*)take(T * GSUM_COLS * 2);
+  S.gs_hs = (uint16_t*)take(T * GSUM_COLS * 2);
+  S.gs_xs = (uint16_t*)take(TK * GSUM_COLS * 2);
+  S.gs_hh = (uint16_t*)take(TK * GSUM_COLS * 2);
   return S;
 }
 
@@ -172,8 +167,10 @@ cudaError_t chunk_make_maps(const MoeLayout& L, const ChunkScratch& S, int Tm, C
   }
   const int TK = Tm * L.K;
   struct Buf { const uint16_t* p; int rows, cols; };
-  const Buf bufs[CM_COUNT] = {{S.xp, Tm, L.H},  {S.xs, TK, L.H},    {S.hs, Tm, L.Is},
-                              {S.hs_lo, Tm, L.Is}, {S.hh, TK, L.I}, {S.hh_lo, TK, L.I}};
+  const Buf bufs[CM_COUNT] = {{S.xp, Tm, L.H},          {S.xs, TK, L.H},          {S.hs, Tm, L.Is},
+                              {S.hs_lo, Tm, L.Is},      {S.hh, TK, L.I},          {S.hh_lo, TK, L.I},
+                              {S.gs_xp, Tm, GSUM_COLS}, {S.gs_xs, TK, GSUM_COLS}, {S.gs_hs, Tm, GSUM_COLS},
+                              {S.gs_hh, TK, GSUM_COLS}};
   const cuuint32_t boxrows[CM_BOXES] = {16, 32, CHUNK_NT};
   for (int b = 0; b < CM_COUNT; ++b)
     for (int v = 0; v < CM_BOXES; ++v) {
@@ -198,10 +195,17 @@ __device__ __forceinline__ float warp_sum_c(float v) {
   return v;
 }
 
+// the group-sum row entries of group g: the fp32 sum as fp16 hi + fp16 remainder
+__device__ __forceinline__ void put_gsum(uint16_t* row, int g, float v) {
+  const __half hi = __float2half_rn(v);
+  const __half lo = __float2half_rn(v - __half2float(hi));
+  *reinterpret_cast<uint32_t*>(row + 2 * g) = (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+}
+
 // x (or RMSNorm(h) * gamma rounded to fp16) -> xp in P8 order, and the sum of each 64-column group of the
-// written values -> sum_xp[g][t]; one warp per token
+// written values -> the token's group-sum row; one warp per token
 __global__ void k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
-                                 int T, int H, uint16_t* __restrict__ xp, float* __restrict__ sum_xp, int sp) {
+                                 int T, int H, uint16_t* __restrict__ xp, uint16_t* __restrict__ gs_xp) {
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (t >= T) return;
   const uint16_t* xr = x + (size_t)t * H;
@@ -233,7 +237,7 @@ __global__ void k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t*
       part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
       part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
       part += __shfl_xor_sync(0xFFFFFFFFu, part, 4);
-      if ((blk & 7) == 0) sum_xp[(size_t)(blk >> 3) * sp + t] = part;
+      if ((blk & 7) == 0) put_gsum(gs_xp + (size_t)t * GSUM_COLS, blk >> 3, part);
       uint4 pk;
       pk.x = o[0] | ((uint32_t)o[1] << 16);
       pk.y = o[2] | ((uint32_t)o[3] << 16);
@@ -357,16 +361,19 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
 }
 
 // xs[row] = xp[tok_of[row]] (fp16 rows of H) and its group sums; one warp per row
-__global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const float* __restrict__ sum_xp, int sp,
+__global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const uint16_t* __restrict__ gs_xp,
                                const int32_t* __restrict__ tok_of, int rows, int H, uint16_t* __restrict__ xs,
-                               float* __restrict__ sum_xs, int sr) {
+                               uint16_t* __restrict__ gs_xs) {
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (r >= rows) return;
   const int t = tok_of[r];
   const uint4* src = reinterpret_cast<const uint4*>(xp + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
   for (int i = lane; i < H / 8; i += 32) dst[i] = src[i];
-  for (int g = lane; g < H / 64; g += 32) sum_xs[(size_t)g * sr + r] = sum_xp[(size_t)g * sp + t];
+  // the 128-byte group-sum row: 8 lanes of 16 bytes
+  if (lane < GSUM_COLS / 8)
+    reinterpret_cast<uint4*>(gs_xs + (size_t)r * GSUM_COLS)[lane] =
+        reinterpret_cast<const uint4*>(gs_xp + (size_t)t * GSUM_COLS)[lane];
 }
 
 // out[t][r] = sum_j w[t][j] * y[slot(t, j)][r] + sg[t] * ys[t][r] (+ h[t][r]), rounded to fp16 once
@@ -394,7 +401,7 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   int n = 0;
   cudaError_t e = cudaMemsetAsync(S.masks, 0, (size_t)E * TW * 4, st);
   if (e != cudaSuccess) return e;
-  k_chunk_prologue<<<(T + 7) / 8, 256, 0, st>>>(x, gamma, eps, T, H, S.xp, S.sum_xp, S.sp);
+  k_chunk_prologue<<<(T + 7) / 8, 256, 0, st>>>(x, gamma, eps, T, H, S.xp, S.gs_xp);
   ++n;
   GemmArgs ga{G, S, T, Tm, 1, status, timeout_ns, nullptr, maps, skip};
   e = chunk_gemm_launch(ga, num_sms, st);
@@ -413,7 +420,7 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   k_chunk_bucket<<<1, BUCKET_THREADS, use_table ? tbl : 0, st>>>(S.masks, E, TW, T, K, S.ids, S.slot_of, S.tok_of,
                                                                  S.groups, S.ctl, use_table);
   ++n;
-  k_chunk_gather<<<(T * K + 7) / 8, 256, 0, st>>>(S.xp, S.sum_xp, S.sp, S.tok_of, T * K, H, S.xs, S.sum_xs, S.sr);
+  k_chunk_gather<<<(T * K + 7) / 8, 256, 0, st>>>(S.xp, S.gs_xp, S.tok_of, T * K, H, S.xs, S.gs_xs);
   ++n;
   ga.phase = 2;
   ga.trace = trace;     // the trace holds the expert gate/up launch

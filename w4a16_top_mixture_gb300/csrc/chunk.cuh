@@ -51,12 +51,11 @@ cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, uint32_t* range
 
 constexpr int CHUNK_NT = 64;   // tokens (rows of activations) per GEMM tile
 
-// scratch of the chunk path for up to Tm tokens. Activation sums are stored K-tile-major, sum[kt][row], with a
-// row stride of sp (token order) or sr (expert-sorted order) floats, both multiples of 4, and SUM_SLACK floats
-// after the last K-tile's run: a K-tile's run for a tile of rows is fetched as SUM_RUN floats from its row
-// rounded down to a multiple of 4 (16-byte aligned bulk copies).
-constexpr int SUM_RUN = 68;
-constexpr int SUM_SLACK = 128;
+// scratch of the chunk path for up to Tm tokens. The group sums of an activation row (the sum of each
+// 64-column group, in fp32) are stored as one 128-byte row of fp16 per activation row: element 2g holds the sum
+// of group g rounded to fp16, element 2g + 1 the remainder rounded to fp16 (hi + lo carries ~22 bits), the rest
+// zero. The GEMM loads a job's rows of them with one TMA tensor load, the B operand of the job's offset term.
+constexpr int GSUM_COLS = 64;   // fp16 per group-sum row: at most 32 groups
 struct ChunkScratch {
   uint16_t* xp;        // [Tm][H] fp16, P8 order (block input, after RMSNorm in residual mode)
   float* logits;       // [Tm][E+1]
@@ -76,18 +75,17 @@ struct ChunkScratch {
   int4* groups;        // [E + Tm*K/CHUNK_NT + 1] (expert, first sorted row, rows) per row tile
   int32_t* ctl;        // [16] ctl[0] row-tile count, ctl[1] rows of the widest row tile; ctl[8] the weight
                        // repack's scale-range flag
-  float* sum_xp;       // [H/64][sp]   sums of xp's rows
-  float* sum_xs;       // [H/64][sr]   sums of xs's rows
-  float* sum_hs;       // [Is/64][sp]  sums of hs + hs_lo / 4096
-  float* sum_hh;       // [I/64][sr]   sums of hh + hh_lo / 4096
-  int sp, sr;          // row strides of the sums
+  uint16_t* gs_xp;     // [Tm][64]   group sums of xp's rows
+  uint16_t* gs_xs;     // [Tm*K][64] group sums of xs's rows
+  uint16_t* gs_hs;     // [Tm][64]   group sums of hs + hs_lo / 4096
+  uint16_t* gs_hh;     // [Tm*K][64] group sums of hh + hh_lo / 4096
 };
 size_t chunk_scratch_bytes(const MoeLayout& L, int Tm);
 ChunkScratch chunk_scratch_carve(const MoeLayout& L, int Tm, uint8_t* base);
 
 // TMA tensor maps of the GEMMs' activation operands: [buffer][box], boxes of 64 columns x 16, 32 or 64 rows,
 // 128-byte swizzle, rows past the buffer read as zero
-enum : int { CM_XP = 0, CM_XS, CM_HS, CM_HSLO, CM_HH, CM_HHLO, CM_COUNT };
+enum : int { CM_XP = 0, CM_XS, CM_HS, CM_HSLO, CM_HH, CM_HHLO, CM_GXP, CM_GXS, CM_GHS, CM_GHH, CM_COUNT };
 constexpr int CM_BOXES = 3;
 struct ChunkMaps {
   CUtensorMap m[CM_COUNT][CM_BOXES];
