@@ -11,18 +11,19 @@
 // projections is h split into fp16 hi + lo/4096 halves; the low halves multiply A1 into a second accumulator
 // (A2's share there is below the fp32 resolution of the sum).
 //
-// Persistent CTAs (one per SM) take jobs j = blockIdx.x + k * gridDim.x. Warp roles, all stepping through the
-// same jobs and K-tiles and handing stages over on mbarriers:
-//   warps 0, 14  producers of the even (warp 0) or odd (warp 14) K-tiles: a bulk copy of the K-tile's weight
-//              block (codes + pairs) and TMA tensor loads of the activation rows (128-byte swizzled K-major),
-//              on the stage's "full" barrier; the producer of a job's first K-tile also loads the job's
-//              group-sum rows into the job's bias tile
+// Persistent CTAs (one per SM, 20 warps) take jobs j = blockIdx.x + k * gridDim.x. Warp roles, all stepping
+// through the same jobs and K-tiles and handing stages over on mbarriers:
+//   warps 0, 18, 19  producers, each of every third K-tile: a bulk copy of the K-tile's weight block (codes +
+//              pairs) and TMA tensor loads of the activation rows (128-byte swizzled K-major), on the stage's
+//              "full" barrier; the producer of a job's first K-tile also loads the job's group-sum rows into
+//              the job's bias tile
 //   warp 1     the MMAs (A from tensor memory, B from shared memory) and their commits; it also owns TMEM. One
 //              thread issues all of the CTA's MMAs and commits: with two issuing threads (alternate K-tiles),
 //              about one forward in thirty at 512 tokens came out with a job at the start of a CTA's work
 //              corrupted.
-//   warps 2-9  dequantise, two groups of four warps taking alternate K-tiles: thread = band row = TMEM lane
-//   warps 10-13 the epilogue of each job (thread = TMEM lane = band row)
+//   warps 2-13 dequantise, three groups of four warps, each taking every third K-tile: thread = band row =
+//              TMEM lane
+//   warps 14-17 the epilogue of each job (thread = TMEM lane = band row)
 // The producer and MMA warps step through their loops as whole warps, so that every copy and MMA operand is
 // warp-uniform, and one elected lane issues the copies or the MMAs: with the loop in one lane, each issue cost
 // that lane several hundred cycles (the MMAs of a K-tile: ~530 traced cycles, now ~75).
@@ -56,7 +57,10 @@ namespace {
 
 enum : int { GK_ROUTER = 0, GK_SHGU = 1, GK_SHDN = 2, GK_EXGU = 3, GK_EXDN = 4 };
 
-constexpr int GTH = 480;                // 15 warps
+constexpr int NDQ = 3;                  // dequantisation groups
+constexpr int NPR = 3;                  // producer warps
+constexpr int GTH = 640;                // 20 warps
+constexpr int WEP = 2 + 4 * NDQ;        // first epilogue warp
 constexpr int NSG_MAX = 16;             // shared-memory stages (the count depends on the phase, see Geo)
 constexpr int NT_MAX = 8;               // A slots in tensor memory (the count depends on the widest job)
 // The stages share one area. A stage is weight block | B hi (up to 64 rows x 128 B, swizzled) | [B lo], each
@@ -276,13 +280,13 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   const uint32_t dcols = lo_phase ? 2 * aw : aw, tlo = aw, ab0 = 2 * dcols, a0 = ab0 + 64;
   const int nt = min(NT_MAX, (int)((512 - a0) / 64));
 
-  if (warp == 0 || warp == 14) {
+  if (warp == 0 || warp >= WEP + 4) {
     // ------------------------------------------------------------------ producers
     // Warp 0 fills the stages of the even K-tiles, warp 14 those of the odd ones. The whole warp steps through
     // the loop, so every copy operand is warp-uniform, and one elected lane arms the stage and issues its
     // copies: the weight block (1-D bulk copy), then B hi and B lo (tensor loads).
-    const uint32_t par = warp == 0 ? 0u : 1u;
-    uint32_t gk = 0, njob = 0;   // njob: jobs whose bias tile was issued (by either producer)
+    const uint32_t par = warp == 0 ? 0u : (uint32_t)(warp - WEP - 3);   // 0, 1, 2
+    uint32_t gk = 0, cyc = 0, njob = 0;   // cyc = gk % NPR; njob: jobs whose bias tile was issued
     bool run = true;
     // test hook: CTA 0 never arms or fills the stage of its first K-tile, so the roles waiting for it time
     // out and the CTA aborts
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       const uint32_t pb = njob & 1u;
       // the job's bias tile, by the producer of its first K-tile, once the bias MMA of job njob - 2 (same
       // buffer) has completed
-      if ((gk & 1u) == par) {
+      if (cyc == par) {
         const bool ok = njob < 2 || wait(&bar->acc_full[pb], ((njob >> 1) - 1) & 1u);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         if (elect_one()) {
@@ -312,7 +316,9 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       }
       ++njob;
       for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sr.next(NSG)) {
-        if ((gk & 1u) != par) continue;
+        const bool mine = cyc == par;
+        cyc = cyc + 1 == (uint32_t)NPR ? 0u : cyc + 1;
+        if (!mine) continue;
         const int s = sr.t;
         const bool ok = gk < NSG || wait(&bar->empty[s], sr.ph ^ 1u);
         if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     if (lane == 0) {
       const uint32_t cnt = gk < (uint32_t)NSG ? gk : (uint32_t)NSG;
       for (uint32_t q = gk - cnt; q < gk; ++q)
-        if ((q & 1u) == par && !(withhold && q == 0)) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
+        if (q % NPR == par && !(withhold && q == 0)) mbar_wait(&bar->full[q % NSG], (q / NSG) & 1u, to);
     }
     for (uint32_t j = njob >= 2 ? njob - 2 : 0; j < njob; ++j) (void)wait(&bar->bb_full[j & 1u], (j >> 1) & 1u);
     __syncwarp();
@@ -400,9 +406,10 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     // the last MMAs must have completed before TMEM is released (a commit tracks all earlier MMAs of its thread)
     if (lane == 0 && gk > 0) mbar_wait(&bar->empty[(gk - 1) % NSG], ((gk - 1) / NSG) & 1u, to);
     __syncwarp();
-  } else if (warp < 10) {
+  } else if (warp < WEP) {
     // ------------------------------------------------------------------ dequantise
-    const int grp = (warp - 2) >> 2;          // this group takes the K-tiles gk with gk % 2 == grp
+    const int grp = (warp - 2) >> 2;          // this group takes the K-tiles gk with gk % NDQ == grp
+    uint32_t cyc = 0;                         // gk % NDQ
     const int r = (warp & 3) * 32 + lane;     // band row = the TMEM lane this warp may access
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const __half2 k1024 = __float2half2_rn(1024.0f), k16 = __float2half2_rn(0.0625f), k64 = __float2half2_rn(-64.0f);
@@ -415,7 +422,9 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     while (run && job_next(g, it, jb)) {
       const uint32_t pb = njob & 1u, tab = trow + ab0 + 32u * pb;
       for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
-        if ((int)(gk & 1u) != grp) continue;
+        const bool mine = (int)cyc == grp;
+        cyc = cyc + 1 == (uint32_t)NDQ ? 0u : cyc + 1;
+        if (!mine) continue;
         const int s = sr.t, t = sl.t;
         // the stage landed; A slot t is free (the MMAs of K-tile gk - nt completed); the bias columns of
         // parity pb are free (the bias MMA of job njob - 2 completed)
@@ -491,7 +500,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       }
       ++njob;
     }
-  } else {
+  } else if (warp < WEP + 4) {
     // ------------------------------------------------------------------ epilogue
     const int q4 = warp & 3;               // TMEM lane quarter this warp may access
     const int r = q4 * 32 + lane;          // band row
