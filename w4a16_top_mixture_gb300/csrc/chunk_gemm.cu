@@ -109,6 +109,11 @@ struct SlotRing {
   __device__ __forceinline__ void next(int nt) {
     if (++t == nt) { t = 0; ph ^= 1u; }
   }
+  // n steps at once, n <= nt
+  __device__ __forceinline__ void adv(int n, int nt) {
+    t += n;
+    if (t >= nt) { t -= nt; ph ^= 1u; }
+  }
 };
 
 // Job j of the phase. Phases 2 and 3 take the expert row-tile count (ngroups) and job j's row-tile entry gr
@@ -282,12 +287,11 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
 
   if (warp == 0 || warp >= WEP + 4) {
     // ------------------------------------------------------------------ producers
-    // Warp 0 fills the stages of the even K-tiles, warp 14 those of the odd ones. The whole warp steps through
-    // the loop, so every copy operand is warp-uniform, and one elected lane arms the stage and issues its
-    // copies: the weight block (1-D bulk copy), then B hi and B lo (tensor loads).
+    // Producer p fills the stages of the K-tiles gk with gk % NPR == p, stepping NPR K-tiles at a time across
+    // job boundaries. The whole warp walks, so every copy operand is warp-uniform, and one elected lane arms
+    // the stage and issues its copies: the weight block (1-D bulk copy), then B hi and B lo (tensor loads).
     const uint32_t par = warp == 0 ? 0u : (uint32_t)(warp - WEP - 3);   // 0, 1, 2
-    uint32_t gk = 0, cyc = 0, njob = 0;   // cyc = gk % NPR; njob: jobs whose bias tile was issued
-    bool run = true;
+    uint32_t gk = 0, njob = 0;   // position in the CTA's K-tile sequence; index of the current job
     // test hook: CTA 0 never arms or fills the stage of its first K-tile, so the roles waiting for it time
     // out and the CTA aborts
     const bool withhold = g.skip && blockIdx.x == 0;
@@ -295,17 +299,27 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     job_begin(g, ngroups, tw, it);
     Job jb;
     SlotRing sr;
-    while (run && job_next(g, it, jb)) {
+    int kt = 0;
+    bool have = job_next(g, it, jb);
+    auto step = [&](int n) {
+      kt += n;
+      gk += (uint32_t)n;
+      sr.adv(n, (int)NSG);
+      while (have && kt >= jb.ktiles) {
+        kt -= jb.ktiles;
+        ++njob;
+        have = job_next(g, it, jb);
+      }
+    };
+    step((int)par);
+    while (have) {
       const int blk = jb.int8 ? GEMM_BLK8 : GEMM_BLK4;
       const int box = box_of(jb.n);
       const bool lo = jb.lomap >= 0;
-      const uint32_t tx = (uint32_t)blk + (16u << box) * 128u * (lo ? 2u : 1u);
-      const CUtensorMap* mhi = &g.maps.m[jb.bmap][box];
-      const CUtensorMap* mlo = &g.maps.m[lo ? jb.lomap : jb.bmap][box];
       const uint32_t pb = njob & 1u;
       // the job's bias tile, by the producer of its first K-tile, once the bias MMA of job njob - 2 (same
       // buffer) has completed
-      if (cyc == par) {
+      if (kt == 0) {
         const bool ok = njob < 2 || wait(&bar->acc_full[pb], ((njob >> 1) - 1) & 1u);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         if (elect_one()) {
@@ -314,25 +328,21 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         }
         __syncwarp();
       }
-      ++njob;
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sr.next(NSG)) {
-        const bool mine = cyc == par;
-        cyc = cyc + 1 == (uint32_t)NPR ? 0u : cyc + 1;
-        if (!mine) continue;
-        const int s = sr.t;
-        const bool ok = gk < NSG || wait(&bar->empty[s], sr.ph ^ 1u);
-        if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
-        if (withhold && gk == 0) continue;
+      const int s = sr.t;
+      const bool ok = gk < NSG || wait(&bar->empty[s], sr.ph ^ 1u);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      if (!(withhold && gk == 0)) {
         uint8_t* st = smem + s * geo.bytes;
         if (elect_one()) {
-          mbar_expect_tx(&bar->full[s], tx);
+          mbar_expect_tx(&bar->full[s], (uint32_t)blk + (16u << box) * 128u * (lo ? 2u : 1u));
           bulk_g2s(st + ST_W, jb.w + (size_t)kt * blk, (uint32_t)blk, &bar->full[s]);
-          tma_load_2d(st + geo.bhi, mhi, kt * 64, jb.row0, &bar->full[s]);
-          if (lo) tma_load_2d(st + geo.blo, mlo, kt * 64, jb.row0, &bar->full[s]);
+          tma_load_2d(st + geo.bhi, &g.maps.m[jb.bmap][box], kt * 64, jb.row0, &bar->full[s]);
+          if (lo) tma_load_2d(st + geo.blo, &g.maps.m[jb.lomap][box], kt * 64, jb.row0, &bar->full[s]);
           GSTAMP(0, gk);
         }
         __syncwarp();
       }
+      step(NPR);
     }
     // drain: every copy this warp issued must have landed before the CTA leaves (the withheld one was never
     // issued); only the last NSG K-tiles can still be in flight, and of the bias tiles those of the last two
@@ -409,30 +419,38 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   } else if (warp < WEP) {
     // ------------------------------------------------------------------ dequantise
     const int grp = (warp - 2) >> 2;          // this group takes the K-tiles gk with gk % NDQ == grp
-    uint32_t cyc = 0;                         // gk % NDQ
     const int r = (warp & 3) * 32 + lane;     // band row = the TMEM lane this warp may access
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const __half2 k1024 = __float2half2_rn(1024.0f), k16 = __float2half2_rn(0.0625f), k64 = __float2half2_rn(-64.0f);
     uint32_t gk = 0, njob = 0;
-    bool run = true;
     JobIter it;
     job_begin(g, ngroups, tw, it);
     Job jb;
     SlotRing sl, sr;
-    while (run && job_next(g, it, jb)) {
-      const uint32_t pb = njob & 1u, tab = trow + ab0 + 32u * pb;
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
-        const bool mine = (int)cyc == grp;
-        cyc = cyc + 1 == (uint32_t)NDQ ? 0u : cyc + 1;
-        if (!mine) continue;
+    // the walk steps NDQ K-tiles at a time, crossing job boundaries as it goes
+    int kt = 0;
+    bool have = job_next(g, it, jb);
+    auto step = [&](int n) {
+      kt += n;
+      gk += (uint32_t)n;
+      sl.adv(n, nt);
+      sr.adv(n, (int)NSG);
+      while (have && kt >= jb.ktiles) {
+        kt -= jb.ktiles;
+        ++njob;
+        have = job_next(g, it, jb);
+      }
+    };
+    step(grp);
+    while (have) {
+      {
+        const uint32_t pb = njob & 1u, tab = trow + ab0 + 32u * pb;
         const int s = sr.t, t = sl.t;
         // the stage landed; A slot t is free (the MMAs of K-tile gk - nt completed); the bias columns of
         // parity pb are free (the bias MMA of job njob - 2 completed)
         if (!wait(&bar->full[s], sr.ph) || (gk >= (uint32_t)nt && !wait(&bar->a_free[t], sl.ph ^ 1u)) ||
-            (njob >= 2 && !wait(&bar->acc_full[pb], ((njob >> 1) - 1) & 1u))) {
-          run = false;
+            (njob >= 2 && !wait(&bar->acc_full[pb], ((njob >> 1) - 1) & 1u)))
           break;
-        }
         tc_fence_after();
         if (r == 0) GSTAMP(1, gk);
         const uint8_t* st = smem + s * geo.bytes + ST_W;
@@ -498,7 +516,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         }
         if (r == 0) GSTAMP(2, gk);
       }
-      ++njob;
+      step(NDQ);
     }
   } else if (warp < WEP + 4) {
     // ------------------------------------------------------------------ epilogue
