@@ -3,6 +3,7 @@
 // See chunk.cuh for the layouts.
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <utility>
 
 #include "chunk.cuh"
 #include "ptx.cuh"
@@ -11,6 +12,29 @@
 namespace moe {
 
 static size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Every kernel of the chunk path is launched programmatic-dependent: its CTAs may become resident while the
+// previous kernel on the stream still runs (once every CTA of that one has run launch_dependents or exited), and
+// each kernel runs griddepcontrol.wait before it reads anything an earlier kernel writes, or writes anything an
+// earlier kernel reads. Only launch latency and set-up overlap; no data is read early.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*k)(KArgs...), int grid, int block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 size_t gemm_store_bytes(const MoeLayout& L) {
   const size_t H = L.H, E = L.E, I = L.I, Is = L.Is, Mr = ((L.E + 1 + 127) / 128) * 128;
@@ -203,41 +227,64 @@ __device__ __forceinline__ void put_gsum(uint16_t* row, int g, float v) {
 }
 
 // x (or RMSNorm(h) * gamma rounded to fp16) -> xp in P8 order, and the sum of each 64-column group of the
-// written values -> the token's group-sum row; one warp per token
-__global__ void k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps,
-                                 int T, int H, uint16_t* __restrict__ xp, uint16_t* __restrict__ gs_xp) {
-  const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
-  if (t >= T) return;
+// written values -> the token's group-sum row. PRO_WPT warps per token, each taking every PRO_WPT-th run of 32
+// 8-column blocks (one 16-byte load per lane); the eight blocks of a group sit on eight neighbouring lanes. With
+// gamma, the token's first warp forms 1 / RMS (the lane-strided sum of squares, then a butterfly) for all four.
+constexpr int PRO_WPT = 4;
+constexpr int PRO_TPC = 2;   // tokens per CTA (PRO_WPT * PRO_TPC warps)
+__global__ void __launch_bounds__(PRO_WPT * PRO_TPC * 32)
+k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, float eps, int T, int H,
+                 uint16_t* __restrict__ xp, uint16_t* __restrict__ gs_xp, uint32_t* __restrict__ masks,
+                 int nmask) {
+  __shared__ float rn_s[PRO_TPC];
+  pdl_wait();
+  pdl_release();
+  // the routing's expert masks start empty
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nmask; i += gridDim.x * blockDim.x) masks[i] = 0u;
+  const int wt = threadIdx.x >> 5, lane = threadIdx.x & 31, tl = wt / PRO_WPT, part = wt % PRO_WPT;
+  const int t = blockIdx.x * PRO_TPC + tl;
+  const bool live = t < T;
   const uint16_t* xr = x + (size_t)t * H;
   float rn = 1.f;
   if (gamma) {
-    float ss = 0.f;
-    for (int i = lane; i < H; i += 32) {
-      const float v = __half2float(__ushort_as_half(xr[i]));
-      ss += v * v;
-    }
-    ss = warp_sum_c(ss);
-    rn = 1.0f / sqrtf(ss / (float)H + eps);
-  }
-  // H / 8 is a multiple of 8, so the 8 blocks of a group sit on 8 neighbouring lanes of one iteration
-  for (int blk = lane; blk < H / 8; blk += 32) {
-    {
-      uint16_t o[8];
-      float part = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = blk * 8 + k;
-        uint16_t v = xr[c];
-        if (gamma)
-          v = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(v)) * rn *
-                                               __half2float(__ushort_as_half(gamma[c]))));
-        o[p8pos(k)] = v;
-        part += __half2float(__ushort_as_half(v));
+    if (live && part == 0) {
+      float ss = 0.f;
+#pragma unroll 8
+      for (int i = lane; i < H; i += 32) {
+        const float v = __half2float(__ushort_as_half(xr[i]));
+        ss += v * v;
       }
-      part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
-      part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
-      part += __shfl_xor_sync(0xFFFFFFFFu, part, 4);
-      if ((blk & 7) == 0) put_gsum(gs_xp + (size_t)t * GSUM_COLS, blk >> 3, part);
+      ss = warp_sum_c(ss);
+      if (lane == 0) rn_s[tl] = 1.0f / sqrtf(ss / (float)H + eps);
+    }
+    __syncthreads();
+    rn = rn_s[tl];
+  }
+  if (!live) return;
+  const int nblk = H / 8;
+#pragma unroll 2
+  for (int base = part * 32; base < nblk; base += 32 * PRO_WPT) {
+    const int blk = base + lane;
+    const bool on = blk < nblk;   // the same for the eight lanes of a group
+    const uint4 raw = on ? *reinterpret_cast<const uint4*>(xr + blk * 8) : make_uint4(0, 0, 0, 0);
+    const uint4 graw = (gamma && on) ? *reinterpret_cast<const uint4*>(gamma + blk * 8) : make_uint4(0, 0, 0, 0);
+    const uint16_t* h8 = reinterpret_cast<const uint16_t*>(&raw);
+    const uint16_t* g8 = reinterpret_cast<const uint16_t*>(&graw);
+    uint16_t o[8];
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint16_t v = h8[k];
+      if (gamma)
+        v = __half_as_ushort(__float2half_rn(__half2float(__ushort_as_half(v)) * rn * __half2float(__ushort_as_half(g8[k]))));
+      o[p8pos(k)] = v;
+      sum += __half2float(__ushort_as_half(v));
+    }
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+    if (on) {
+      if ((blk & 7) == 0) put_gsum(gs_xp + (size_t)t * GSUM_COLS, blk >> 3, sum);
       uint4 pk;
       pk.x = o[0] | ((uint32_t)o[1] << 16);
       pk.y = o[2] | ((uint32_t)o[3] << 16);
@@ -256,6 +303,8 @@ template <int EPL>
 __global__ void k_chunk_route(const float* __restrict__ logits, int E, int K, int T, int32_t* __restrict__ ids,
                               float* __restrict__ w, float* __restrict__ sg, uint32_t* __restrict__ masks, int TW,
                               int32_t* rec_ids, float* rec_w, float* rec_sg) {
+  pdl_wait();
+  pdl_release();
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* lg = logits + (size_t)t * (E + 1);
@@ -296,6 +345,8 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
                                                                  int32_t* __restrict__ ctl, int use_table) {
   extern __shared__ int pre[];   // [E][TW] when use_table
   __shared__ int cnt[512], off[512], goff[512], wsum[32], wgsum[32], wmax[32];
+  pdl_wait();
+  pdl_release();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
   // counts (thread = expert) and the prefix table
   int c = 0;
@@ -344,19 +395,40 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
   for (int e = tid; e < E; e += blockDim.x)
     for (int g = 0; g * CHUNK_NT < cnt[e]; ++g)
       groups[goff[e] + g] = make_int4(e, off[e] + g * CHUNK_NT, min(CHUNK_NT, cnt[e] - g * CHUNK_NT), 0);
-  for (int p = tid; p < T * K; p += blockDim.x) {
-    const int t = p / K, e = ids[p];
-    const uint32_t* m = masks + (size_t)e * TW;
-    int rank = 0;
-    if (use_table) {
-      rank = pre[e * TW + (t >> 5)];
-    } else {
-      for (int q = 0; q < (t >> 5); ++q) rank += __popc(m[q]);
+  // the (token, slot) pairs, four a thread at a time: the four ids, then the four mask words, are loaded before
+  // any is used (each pass is two dependent global loads, not eight)
+  const int TKp = T * K;
+  for (int p0 = tid; p0 < TKp; p0 += 4 * blockDim.x) {
+    int e[4];
+    uint32_t mw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = p0 + u * blockDim.x;
+      e[u] = p < TKp ? ids[p] : 0;
     }
-    rank += __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
-    const int row = off[e] + rank;
-    slot_of[p] = row;
-    tok_of[row] = t;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = p0 + u * blockDim.x;
+      mw[u] = p < TKp ? masks[(size_t)e[u] * TW + ((p / K) >> 5)] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = p0 + u * blockDim.x;
+      if (p < TKp) {
+        const int t = p / K;
+        int rank = 0;
+        if (use_table) {
+          rank = pre[e[u] * TW + (t >> 5)];
+        } else {
+          const uint32_t* m = masks + (size_t)e[u] * TW;
+          for (int q = 0; q < (t >> 5); ++q) rank += __popc(m[q]);
+        }
+        rank += __popc(mw[u] & ((1u << (t & 31)) - 1u));
+        const int row = off[e[u]] + rank;
+        slot_of[p] = row;
+        tok_of[row] = t;
+      }
+    }
   }
 }
 
@@ -364,31 +436,86 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
 __global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const uint16_t* __restrict__ gs_xp,
                                const int32_t* __restrict__ tok_of, int rows, int H, uint16_t* __restrict__ xs,
                                uint16_t* __restrict__ gs_xs) {
+  pdl_wait();
+  pdl_release();
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (r >= rows) return;
   const int t = tok_of[r];
   const uint4* src = reinterpret_cast<const uint4*>(xp + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
-  for (int i = lane; i < H / 8; i += 32) dst[i] = src[i];
+  // eight 16-byte loads a lane in flight before the stores
+  for (int b0 = 0; b0 < H / 8; b0 += 256) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = b0 + k * 32 + lane;
+      v[k] = i < H / 8 ? src[i] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = b0 + k * 32 + lane;
+      if (i < H / 8) dst[i] = v[k];
+    }
+  }
   // the 128-byte group-sum row: 8 lanes of 16 bytes
   if (lane < GSUM_COLS / 8)
     reinterpret_cast<uint4*>(gs_xs + (size_t)r * GSUM_COLS)[lane] =
         reinterpret_cast<const uint4*>(gs_xp + (size_t)t * GSUM_COLS)[lane];
 }
 
-// out[t][r] = sum_j w[t][j] * y[slot(t, j)][r] + sg[t] * ys[t][r] (+ h[t][r]), rounded to fp16 once
+// out[t][r] = sum_j w[t][j] * y[slot(t, j)][r] + sg[t] * ys[t][r] (+ h[t][r]), rounded to fp16 once. A thread
+// takes four neighbouring columns of one token: its K slots and weights first, then the K rows' 16-byte loads,
+// so that the loads are in flight together; every column adds its terms in the order above. KM >= K bounds the
+// per-thread arrays.
+template <int KM>
 __global__ void k_chunk_combine(const float* __restrict__ y, const float* __restrict__ ys,
                                 const int32_t* __restrict__ slot_of, const float* __restrict__ w,
                                 const float* __restrict__ sg, const uint16_t* __restrict__ resid, int T, int H,
                                 int K, uint16_t* __restrict__ out) {
-  const size_t n = (size_t)T * H;
+  pdl_wait();
+  pdl_release();
+  const int H4 = H / 4;
+  const size_t n = (size_t)T * H4;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / H), r = (int)(i % H);
-    float acc = 0.f;
-    for (int j = 0; j < K; ++j) acc += w[(size_t)t * K + j] * y[(size_t)slot_of[(size_t)t * K + j] * H + r];
-    acc += sg[t] * ys[i];
-    if (resid) acc += __half2float(__ushort_as_half(resid[i]));
-    out[i] = __half_as_ushort(__float2half_rn(acc));
+    const int t = (int)(i / H4), c = (int)(i % H4) * 4;
+    int sl[KM];
+    float wv[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < K) {
+        sl[j] = slot_of[(size_t)t * K + j];
+        wv[j] = w[(size_t)t * K + j];
+      }
+    float4 yv[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < K) yv[j] = *reinterpret_cast<const float4*>(y + (size_t)sl[j] * H + c);
+    const float4 sv = *reinterpret_cast<const float4*>(ys + (size_t)t * H + c);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < K) {
+        a0 += wv[j] * yv[j].x;
+        a1 += wv[j] * yv[j].y;
+        a2 += wv[j] * yv[j].z;
+        a3 += wv[j] * yv[j].w;
+      }
+    const float g = sg[t];
+    a0 += g * sv.x;
+    a1 += g * sv.y;
+    a2 += g * sv.z;
+    a3 += g * sv.w;
+    if (resid) {
+      const uint2 rr = *reinterpret_cast<const uint2*>(resid + (size_t)t * H + c);
+      a0 += __half2float(__ushort_as_half((uint16_t)(rr.x & 0xFFFFu)));
+      a1 += __half2float(__ushort_as_half((uint16_t)(rr.x >> 16)));
+      a2 += __half2float(__ushort_as_half((uint16_t)(rr.y & 0xFFFFu)));
+      a3 += __half2float(__ushort_as_half((uint16_t)(rr.y >> 16)));
+    }
+    uint2 o;
+    o.x = (uint32_t)__half_as_ushort(__float2half_rn(a0)) | ((uint32_t)__half_as_ushort(__float2half_rn(a1)) << 16);
+    o.y = (uint32_t)__half_as_ushort(__float2half_rn(a2)) | ((uint32_t)__half_as_ushort(__float2half_rn(a3)) << 16);
+    *reinterpret_cast<uint2*>(out + (size_t)t * H + c) = o;
   }
 }
 
@@ -399,9 +526,9 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
                           uint64_t* trace, cudaStream_t st, int* launches, int skip) {
   const int E = L.E, K = L.K, H = L.H, TW = (T + 31) / 32;
   int n = 0;
-  cudaError_t e = cudaMemsetAsync(S.masks, 0, (size_t)E * TW * 4, st);
+  cudaError_t e = launch_pdl(k_chunk_prologue, (T + PRO_TPC - 1) / PRO_TPC, PRO_WPT * PRO_TPC * 32, 0, st, x, gamma,
+                             eps, T, H, S.xp, S.gs_xp, S.masks, E * TW);
   if (e != cudaSuccess) return e;
-  k_chunk_prologue<<<(T + 7) / 8, 256, 0, st>>>(x, gamma, eps, T, H, S.xp, S.gs_xp);
   ++n;
   GemmArgs ga{G, S, T, Tm, 1, status, timeout_ns, nullptr, maps, skip};
   e = chunk_gemm_launch(ga, num_sms, st);
@@ -411,16 +538,21 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   {
     auto* route = E <= 32 ? k_chunk_route<1> : E <= 64 ? k_chunk_route<2> : E <= 128 ? k_chunk_route<4>
                   : E <= 256 ? k_chunk_route<8> : k_chunk_route<16>;
-    route<<<(T + 7) / 8, 256, 0, st>>>(S.logits, E, K, T, S.ids, S.w, S.sg, S.masks, TW, rec_ids, rec_w, rec_sg);
+    e = launch_pdl(route, (T + 7) / 8, 256, 0, st, (const float*)S.logits, E, K, T, S.ids, S.w, S.sg, S.masks, TW,
+                   rec_ids, rec_w, rec_sg);
+    if (e != cudaSuccess) return e;
   }
   ++n;
   // the prefix table fits in shared memory for chunks up to tens of thousands of tokens
   const size_t tbl = (size_t)E * TW * sizeof(int);
   const int use_table = tbl <= BUCKET_TABLE_MAX ? 1 : 0;
-  k_chunk_bucket<<<1, BUCKET_THREADS, use_table ? tbl : 0, st>>>(S.masks, E, TW, T, K, S.ids, S.slot_of, S.tok_of,
-                                                                 S.groups, S.ctl, use_table);
+  e = launch_pdl(k_chunk_bucket, 1, BUCKET_THREADS, use_table ? tbl : 0, st, (const uint32_t*)S.masks, E, TW, T, K,
+                 (const int32_t*)S.ids, S.slot_of, S.tok_of, S.groups, S.ctl, use_table);
+  if (e != cudaSuccess) return e;
   ++n;
-  k_chunk_gather<<<(T * K + 7) / 8, 256, 0, st>>>(S.xp, S.gs_xp, S.tok_of, T * K, H, S.xs, S.gs_xs);
+  e = launch_pdl(k_chunk_gather, (T * K + 7) / 8, 256, 0, st, (const uint16_t*)S.xp, (const uint16_t*)S.gs_xp,
+                 (const int32_t*)S.tok_of, T * K, H, S.xs, S.gs_xs);
+  if (e != cudaSuccess) return e;
   ++n;
   ga.phase = 2;
   ga.trace = trace;     // the trace holds the expert gate/up launch
@@ -432,9 +564,12 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   e = chunk_gemm_launch(ga, num_sms, st);
   if (e != cudaSuccess) return e;
   ++n;
-  const size_t tot = (size_t)T * H;
+  const size_t tot = (size_t)T * (H / 4);
   const int cg = (int)((tot + 255) / 256 < 65536 ? (tot + 255) / 256 : 65536);
-  k_chunk_combine<<<cg, 256, 0, st>>>(S.y, S.ys, S.slot_of, S.w, S.sg, gamma ? x : nullptr, T, H, K, out);
+  auto* combine = K <= 8 ? k_chunk_combine<8> : k_chunk_combine<16>;
+  e = launch_pdl(combine, cg, 256, 0, st, (const float*)S.y, (const float*)S.ys, (const int32_t*)S.slot_of,
+                 (const float*)S.w, (const float*)S.sg, gamma ? x : (const uint16_t*)nullptr, T, H, K, out);
+  if (e != cudaSuccess) return e;
   ++n;
   if (launches) *launches = n;
   return cudaGetLastError();

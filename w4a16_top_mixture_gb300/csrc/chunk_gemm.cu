@@ -263,13 +263,19 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     }
     mbar_init(&bar->fold_sync, 4);
     bar->abort = 0;
+  }
+  if (warp == 1) { tmem_alloc(&bar->tslot, 512); tmem_relinquish(); }
+  // programmatic-dependent launch: everything above overlaps the previous kernel; from here on its outputs are
+  // read (the bucketing's tile list, the activations)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) {
     // phase 1 tiles the tokens 64 at a time; phases 2 and 3 take the bucketing's row tiles, and phase 3 tiles
     // the shared down's tokens as wide as the widest row tile, so no job is wider than that
     bar->ngroups = g.phase == 1 ? 0 : g.S.ctl[0];
     bar->tw = g.phase == 1 ? CHUNK_NT : min(CHUNK_NT, max(16, (g.S.ctl[1] + 15) & ~15));
     fence_mbar_init();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
-  if (warp == 1) { tmem_alloc(&bar->tslot, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -643,8 +649,18 @@ cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
       configured[dev] = true;
     }
   }
-  k_chunk_gemm<<<grid, GTH, GEMM_SMEM, st>>>(g);
-  return cudaGetLastError();
+  // programmatic-dependent: the CTAs set up their barriers and tensor memory while the previous kernel ends
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(GTH);
+  cfg.dynamicSmemBytes = GEMM_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_chunk_gemm, g);
 }
 
 }  // namespace moe
