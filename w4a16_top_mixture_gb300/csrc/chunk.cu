@@ -137,7 +137,7 @@ size_t chunk_scratch_bytes(const MoeLayout& L, int Tm) {
   const size_t H = L.H, E = L.E, K = L.K, I = L.I, Is = L.Is, T = Tm, TK = (size_t)Tm * L.K;
   const size_t TW = (T + 31) / 32;
   size_t b = 0;
-  b += al256(T * H * 2) + al256(T * (E + 1) * 4);
+  b += al256(T * H * 2) + al256(ROUTER_SPLIT * T * logit_stride((int)E) * 4);
   b += al256(T * Is * 2) * 2 + al256(T * H * 4);
   b += al256(T * K * 4) * 2 + al256(T * 4) + al256(E * TW * 4) + al256(T * K * 4) + al256(TK * 4);
   b += al256(TK * H * 2);
@@ -154,7 +154,7 @@ ChunkScratch chunk_scratch_carve(const MoeLayout& L, int Tm, uint8_t* base) {
   auto take = [&](size_t n) { uint8_t* r = p; p += al256(n); return r; };
   ChunkScratch S;
   S.xp = (uint16_t*)take(T * H * 2);
-  S.logits = (float*)take(T * (E + 1) * 4);
+  S.logits = (float*)take(ROUTER_SPLIT * T * logit_stride((int)E) * 4);
   S.hs = (uint16_t*)take(T * Is * 2);
   S.hs_lo = (uint16_t*)take(T * Is * 2);
   S.ys = (float*)take(T * H * 4);
@@ -300,17 +300,54 @@ k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
 // 32 * EPL >= E. The ids are below E whatever the logits hold (NaN and infinities included), so the masks and
 // everything indexed by an id stay in bounds.
 template <int EPL>
-__global__ void k_chunk_route(const float* __restrict__ logits, int E, int K, int T, int32_t* __restrict__ ids,
-                              float* __restrict__ w, float* __restrict__ sg, uint32_t* __restrict__ masks, int TW,
-                              int32_t* rec_ids, float* rec_w, float* rec_sg) {
+__global__ void k_chunk_route(const float* __restrict__ logits, int np, int E, int K, int T,
+                              int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ sg,
+                              uint32_t* __restrict__ masks, int TW, int32_t* rec_ids, float* rec_w, float* rec_sg) {
   pdl_wait();
   pdl_release();
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (t >= T) return;
-  const float* lg = logits + (size_t)t * (E + 1);
+  // the logits: the router GEMM's np partial sums, added in part order. Rows are logit_stride(E) floats, so
+  // with E a multiple of 128 each lane's EPL logits are whole float4s (all loads issued before the adds)
+  const int LS = logit_stride(E);
+  const size_t pstride = (size_t)T * LS;
+  const float* lg = logits + (size_t)t * LS;
+  uint32_t key[EPL];
+  if (EPL % 4 == 0 && E == 32 * EPL) {
+    constexpr int Q = EPL / 4 > 0 ? EPL / 4 : 1;
+    float4 v[ROUTER_SPLIT][Q];
+#pragma unroll
+    for (int p = 0; p < ROUTER_SPLIT; ++p)
+#pragma unroll
+      for (int q = 0; q < Q; ++q)
+        if (p < np) v[p][q] = __ldcg(reinterpret_cast<const float4*>(lg + p * pstride + lane * EPL) + q);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      float4 a = v[0][q];
+#pragma unroll
+      for (int p = 1; p < ROUTER_SPLIT; ++p)
+        if (p < np) { a.x += v[p][q].x; a.y += v[p][q].y; a.z += v[p][q].z; a.w += v[p][q].w; }
+      key[4 * q] = topk_key(a.x);
+      key[4 * q + 1] = topk_key(a.y);
+      key[4 * q + 2] = topk_key(a.z);
+      key[4 * q + 3] = topk_key(a.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane * EPL + i;
+      float v = 0.f;
+      if (e < E) {
+        v = __ldcg(lg + e);
+        for (int p = 1; p < np; ++p) v += __ldcg(lg + p * pstride + e);
+      }
+      key[i] = e < E ? topk_key(v) : 0u;
+    }
+  }
   int sel_idx;
-  float sel_val;
-  warp_topk_lean<EPL, false>(lg, E, K, sel_idx, sel_val);
+  uint32_t sel_key;
+  warp_topk_keys<EPL>(key, K, sel_idx, sel_key);
+  const float sel_val = topk_logit(sel_key);
   const float mx = __shfl_sync(0xFFFFFFFFu, sel_val, 0);
   const float ex = lane < K ? __expf(sel_val - mx) : 0.f;
   const float z = warp_sum_c(ex);
@@ -324,7 +361,9 @@ __global__ void k_chunk_route(const float* __restrict__ logits, int E, int K, in
     atomicOr(&masks[(size_t)sel_idx * TW + (t >> 5)], 1u << (t & 31));
   }
   if (lane == 0) {
-    const float g = __frcp_rn(1.0f + __expf(-lg[E]));
+    float gl = __ldcg(lg + E);
+    for (int p = 1; p < np; ++p) gl += __ldcg(lg + p * pstride + E);
+    const float g = __frcp_rn(1.0f + __expf(-gl));
     sg[t] = g;
     if (rec_sg) rec_sg[t] = g;
   }
@@ -538,8 +577,8 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
   {
     auto* route = E <= 32 ? k_chunk_route<1> : E <= 64 ? k_chunk_route<2> : E <= 128 ? k_chunk_route<4>
                   : E <= 256 ? k_chunk_route<8> : k_chunk_route<16>;
-    e = launch_pdl(route, (T + 7) / 8, 256, 0, st, (const float*)S.logits, E, K, T, S.ids, S.w, S.sg, S.masks, TW,
-                   rec_ids, rec_w, rec_sg);
+    e = launch_pdl(route, (T + 7) / 8, 256, 0, st, (const float*)S.logits, router_parts(H / 64), E, K, T, S.ids,
+                   S.w, S.sg, S.masks, TW, rec_ids, rec_w, rec_sg);
     if (e != cudaSuccess) return e;
   }
   ++n;

@@ -16,12 +16,12 @@
 // yield the column pairs (k, 4+k) of an 8-column block; activations are stored in the matching order
 // (0 4 1 5 2 6 3 7 per 8 columns, "P8"), which leaves every dot product unchanged.
 //
-// The GEMM multiplies the exact integer codes (as fp16) by the activations on the tensor cores, one K-tile
-// (one group) at a time into a fresh accumulator, and folds each K-tile in fp32: acc += s * D + b * sum(x),
-// with sum(x) the activations' sum over the tile's 64 columns. Activation tiles arrive by TMA tensor loads
-// (128-byte swizzled, the layout the MMA reads) through tensor maps made once per handle. The sums are made once
-// per activation row by the kernel that writes the row (the prologue, the gather, the SwiGLU epilogue) and kept
-// K-tile-major, sum[kt][row], so that one K-tile's sums for a tile of rows are one short contiguous run.
+// The GEMM (chunk_gemm.cu) forms each K-tile's scaled codes s * q as an exact pair of fp16 halves A1 + A2 in
+// tensor memory and accumulates A1 x + A2 x for a whole job in one fp32 accumulator; the offset term
+// sum_g b_g sum(x over group g) is one more MMA per job against the activation rows' group sums. The group sums
+// are made once per activation row by the kernel that writes the row (the prologue, the gather, the SwiGLU
+// epilogue), as one 128-byte row of fp16 hi + lo pairs. Activation tiles and group-sum rows arrive by TMA tensor
+// loads (128-byte swizzled, the layout the MMA reads) through tensor maps made once per handle.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -50,6 +50,14 @@ GemmLayout gemm_layout_carve(const MoeLayout& L, uint8_t* base);
 cudaError_t gemm_repack(const RepackSrc& w, const GemmLayout& G, uint32_t* range_bad, cudaStream_t st);
 
 constexpr int CHUNK_NT = 64;   // tokens (rows of activations) per GEMM tile
+// The router's GEMM is split along K into up to ROUTER_SPLIT parts of a multiple of 8 K-tiles each (the offset
+// term's MMA takes 8 groups per K step), each part a job of its own writing partial logits; the routing adds
+// the parts in order.
+constexpr int ROUTER_SPLIT = 4;
+__host__ __device__ constexpr int router_kpp(int kt) { return (((kt + ROUTER_SPLIT - 1) / ROUTER_SPLIT) + 7) & ~7; }
+__host__ __device__ constexpr int router_parts(int kt) { return (kt + router_kpp(kt) - 1) / router_kpp(kt); }
+// row stride (floats) of the partial logits: E + 1 rounded up to 4, so that a lane reads its logits as float4s
+__host__ __device__ constexpr int logit_stride(int e) { return (e + 1 + 3) & ~3; }
 
 // scratch of the chunk path for up to Tm tokens. The group sums of an activation row (the sum of each
 // 64-column group, in fp32) are stored as one 128-byte row of fp16 per activation row: element 2g holds the sum
@@ -58,7 +66,7 @@ constexpr int CHUNK_NT = 64;   // tokens (rows of activations) per GEMM tile
 constexpr int GSUM_COLS = 64;   // fp16 per group-sum row: at most 32 groups
 struct ChunkScratch {
   uint16_t* xp;        // [Tm][H] fp16, P8 order (block input, after RMSNorm in residual mode)
-  float* logits;       // [Tm][E+1]
+  float* logits;       // [parts][T][logit_stride(E)] partial router logits (parts = router_parts(H / 64))
   uint16_t* hs;        // [Tm][Is] fp16, P8 order: RN_fp16(h) of the shared expert
   uint16_t* hs_lo;     // [Tm][Is] fp16, P8 order: RN_fp16(4096 (h - hs)), the low half of the split
   float* ys;           // [Tm][H] shared-expert output
@@ -92,7 +100,7 @@ struct ChunkMaps {
 };
 cudaError_t chunk_make_maps(const MoeLayout& L, const ChunkScratch& S, int Tm, ChunkMaps* out);
 
-// GEMM launch of one phase: 1 router + shared gate/up, 2 expert gate/up, 3 expert down + shared down
+// GEMM launch of one phase: 1 router (in K parts), 2 expert + shared gate/up, 3 expert down + shared down
 struct GemmArgs {
   GemmLayout G;
   ChunkScratch S;

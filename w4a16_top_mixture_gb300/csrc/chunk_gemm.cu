@@ -72,12 +72,11 @@ struct Geo {
   int nsg, bytes, bhi, blo;
 };
 __host__ __device__ constexpr Geo geo_of(int phase) {
-  return phase == 1 ? Geo{10, 17408, 9216, 9216}       // int8 router / shared gate-up blocks, B hi
-         : phase == 2 ? Geo{13, 13312, 5120, 5120}     // int4 expert gate/up blocks, B hi
-                      : Geo{7, 25600, 9216, 17408};    // int4 / int8 down blocks, B hi and lo
+  return phase != 3 ? Geo{10, 17408, 9216, 9216}       // int8 router; int4 expert / int8 shared gate/up; B hi
+                    : Geo{7, 25600, 9216, 17408};      // int4 / int8 down blocks, B hi and lo
 }
 static_assert(geo_of(1).nsg * geo_of(1).bytes <= ST_AREA && geo_of(2).nsg * geo_of(2).bytes <= ST_AREA &&
-                  geo_of(3).nsg * geo_of(3).bytes <= ST_AREA && geo_of(2).nsg <= NSG_MAX,
+                  geo_of(3).nsg * geo_of(3).bytes <= ST_AREA && geo_of(1).nsg <= NSG_MAX,
               "stages");
 static_assert(GEMM_BLK8 <= 9216 && GEMM_BLK4 <= 5120, "weight block fits before B");
 static_assert(GSUM_COLS * 2 == 128, "a group-sum row is one 128-byte swizzle row");
@@ -96,6 +95,7 @@ struct Job {
   int kind, m, e;
   const uint8_t* w;       // weight block of K-tile 0 of the band
   int ktiles, int8;
+  int k0, part;           // the job's first K-tile and K part (the router's split; 0 otherwise)
   int bmap, lomap;        // tensor maps of the activations and of their low halves (-1: none)
   int row0, cnt, n;       // first activation row, rows, MMA N (cnt rounded up to 16)
   int gmap;               // tensor map of the activation rows' group sums
@@ -118,30 +118,30 @@ struct SlotRing {
 
 // Job j of the phase. Phases 2 and 3 take the expert row-tile count (ngroups) and job j's row-tile entry gr
 // (S.groups[j % ngroups] for the expert jobs) from the caller, which loads them ahead of time.
-// Token tiles (phase 1, and the shared down of phase 3) are tw rows wide.
+// Phase 1: the router bands by token tile (tw = CHUNK_NT rows) and K part. Phase 2: the expert gate/up jobs,
+// then the shared gate/up bands by token tiles of CHUNK_NT. Phase 3: the expert down jobs, then the shared down
+// bands by token tiles of tw rows.
 __device__ __forceinline__ bool decode_job(const GemmArgs& g, int j, int ngroups, int tw, int4 gr, Job& jb) {
   const GemmLayout& G = g.G;
   const int H = G.H, I = G.I, Is = G.Is, T = g.T;
   const int NTT = (T + tw - 1) / tw;
   jb.e = 0;
   jb.lomap = -1;
+  jb.k0 = 0;
+  jb.part = 0;
   auto token_tile = [&](int nt) {
     jb.row0 = nt * tw;
     jb.cnt = min(tw, T - jb.row0);
   };
   if (g.phase == 1) {
-    const int MTr = G.Mr / 128, MTs = 2 * Is / 128;
-    if (j < MTr * NTT) {
-      jb.kind = GK_ROUTER; jb.m = j % MTr; token_tile(j / MTr);
-      jb.w = G.gr + (size_t)jb.m * (H / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = H / 64;
-      jb.bmap = CM_XP; jb.gmap = CM_GXP;
-    } else {
-      j -= MTr * NTT;
-      if (j >= MTs * NTT) return false;
-      jb.kind = GK_SHGU; jb.m = j % MTs; token_tile(j / MTs);
-      jb.w = G.gsgu + (size_t)jb.m * (H / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = H / 64;
-      jb.bmap = CM_XP; jb.gmap = CM_GXP;
-    }
+    // the router bands, each token tile's K cut into router_parts parts (jobs of their own)
+    const int MTr = G.Mr / 128, KT = H / 64, kpp = router_kpp(KT), NP = router_parts(KT);
+    if (j >= MTr * NTT * NP) return false;
+    const int rest = j / MTr;
+    jb.kind = GK_ROUTER; jb.m = j % MTr; token_tile(rest % NTT);
+    jb.part = rest / NTT; jb.k0 = jb.part * kpp; jb.ktiles = min(kpp, KT - jb.k0);
+    jb.w = G.gr + (size_t)jb.m * KT * GEMM_BLK8; jb.int8 = 1;
+    jb.bmap = CM_XP; jb.gmap = CM_GXP;
   } else {
     const int MTg = 2 * I / 128, MTd = H / 128;
     const int nex = (g.phase == 2 ? MTg : MTd) * ngroups;   // expert jobs; phase 3 then the shared down
@@ -159,9 +159,19 @@ __device__ __forceinline__ bool decode_job(const GemmArgs& g, int j, int ngroups
         jb.w = G.gedn + (size_t)gr.x * G.gedn_expert + (size_t)m * (I / 64) * GEMM_BLK4; jb.ktiles = I / 64;
         jb.bmap = CM_HH; jb.lomap = CM_HHLO; jb.gmap = CM_GHH;
       }
+    } else if (g.phase == 2) {
+      // then the shared expert's gate/up bands, in token tiles of CHUNK_NT
+      j -= nex;
+      const int MTs = 2 * Is / 128, NTS = (T + CHUNK_NT - 1) / CHUNK_NT;
+      if (j >= MTs * NTS) return false;
+      jb.kind = GK_SHGU; jb.m = j % MTs;
+      jb.row0 = (j / MTs) * CHUNK_NT;
+      jb.cnt = min(CHUNK_NT, T - jb.row0);
+      jb.w = G.gsgu + (size_t)jb.m * (H / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = H / 64;
+      jb.bmap = CM_XP; jb.gmap = CM_GXP;
     } else {
       j -= nex;
-      if (g.phase != 3 || j >= MTd * NTT) return false;
+      if (j >= MTd * NTT) return false;
       jb.kind = GK_SHDN; jb.m = j % MTd; token_tile(j / MTd);
       jb.w = G.gsdn + (size_t)jb.m * (Is / 64) * GEMM_BLK8; jb.int8 = 1; jb.ktiles = Is / 64;
       jb.bmap = CM_HS; jb.lomap = CM_HSLO; jb.gmap = CM_GHS;
@@ -287,7 +297,10 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   // up to 32), in phase 3 aw more for the low halves; the bias A operands (job parity, 32 columns: column g
   // holds the pair (b_g, b_g)); the A slots (64 columns: A1 | A2)
   const bool lo_phase = g.phase == 3;
-  const uint32_t aw = (uint32_t)((min(tw, g.phase == 1 ? ((min(g.T, CHUNK_NT) + 15) & ~15) : CHUNK_NT) + 31) & ~31);
+  // the widest job: phase 1 token tiles of up to CHUNK_NT; phase 2 the expert row tiles (tw) and the shared
+  // gate/up token tiles of up to CHUNK_NT; phase 3 tw
+  const int tok_w = (min(g.T, CHUNK_NT) + 15) & ~15;
+  const uint32_t aw = (uint32_t)(((g.phase == 1 ? tok_w : g.phase == 2 ? max(tw, tok_w) : tw) + 31) & ~31);
   const uint32_t dcols = lo_phase ? 2 * aw : aw, tlo = aw, ab0 = 2 * dcols, a0 = ab0 + 64;
   const int nt = min(NT_MAX, (int)((512 - a0) / 64));
 
@@ -341,9 +354,10 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         uint8_t* st = smem + s * geo.bytes;
         if (elect_one()) {
           mbar_expect_tx(&bar->full[s], (uint32_t)blk + (16u << box) * 128u * (lo ? 2u : 1u));
-          bulk_g2s(st + ST_W, jb.w + (size_t)kt * blk, (uint32_t)blk, &bar->full[s]);
-          tma_load_2d(st + geo.bhi, &g.maps.m[jb.bmap][box], kt * 64, jb.row0, &bar->full[s]);
-          if (lo) tma_load_2d(st + geo.blo, &g.maps.m[jb.lomap][box], kt * 64, jb.row0, &bar->full[s]);
+          const int kg = jb.k0 + kt;   // K-tile within the band
+          bulk_g2s(st + ST_W, jb.w + (size_t)kg * blk, (uint32_t)blk, &bar->full[s]);
+          tma_load_2d(st + geo.bhi, &g.maps.m[jb.bmap][box], kg * 64, jb.row0, &bar->full[s]);
+          if (lo) tma_load_2d(st + geo.blo, &g.maps.m[jb.lomap][box], kg * 64, jb.row0, &bar->full[s]);
           GSTAMP(0, gk);
         }
         __syncwarp();
@@ -409,8 +423,8 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
           if (last) {
             // the offset term: D += (b_g, b_g) . (sum_hi_g, sum_lo_g) over the job's groups, 8 groups per
             // K step; the bias columns past the job's groups are zero
-            const int nbk = (jb.ktiles + 7) >> 3;
-            for (int ks = 0; ks < nbk; ++ks) umma_f16_ts(d, ab + 8 * ks, bb + 2 * ks, idesc, 1u);
+            const int nbk = (jb.ktiles + 7) >> 3, kb0 = jb.k0 >> 3;   // k0: a multiple of 8 groups
+            for (int ks = 0; ks < nbk; ++ks) umma_f16_ts(d, ab + 8 * ks, bb + 2 * (kb0 + ks), idesc, 1u);
             umma_commit(&bar->acc_full[pb]);
           }
           GSTAMP(3, gk);
@@ -581,7 +595,8 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         const int er = jb.m * 128 + r;
         if (er <= G.E)
 #pragma unroll 4
-          for (int i = 0; i < cnt; ++i) S.logits[(size_t)(jb.row0 + i) * (G.E + 1) + er] = ep[r * 65 + i];
+          for (int i = 0; i < cnt; ++i)
+            S.logits[((size_t)jb.part * g.T + jb.row0 + i) * logit_stride(G.E) + er] = ep[r * 65 + i];
       } else if (jb.kind == GK_SHDN || jb.kind == GK_EXDN) {
         float* dst = jb.kind == GK_SHDN ? S.ys : S.y;
 #pragma unroll 4
