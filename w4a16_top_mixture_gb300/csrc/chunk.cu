@@ -369,106 +369,85 @@ __global__ void k_chunk_route(const float* __restrict__ logits, int np, int E, i
   }
 }
 
-// One CTA of BUCKET_THREADS: per-expert token counts from the masks, exclusive scan, the sorted row of every
-// (token, slot), the token of every sorted row, and the list of row tiles (expert, first row, rows <= CHUNK_NT);
-// ctl[0] = tile count, ctl[1] = rows of the widest tile. Tokens of an expert keep their order. With a prefix
-// table (dynamic shared memory of E * TW ints: the tokens of expert e in mask words before word q), a pair's
-// rank is one table read and one mask word; without it (very long chunks) the rank counts the earlier words.
-constexpr int BUCKET_THREADS = 1024;
-constexpr size_t BUCKET_TABLE_MAX = 40960;   // prefix-table bytes that fit beside the static arrays in 48 KB
+// One CTA per expert e (BUCKET_THREADS threads). Every CTA counts the tokens of every expert from the masks
+// (thread = expert) and reduces: its expert's first sorted row (the tokens of the experts before it), its first
+// row tile, and, in CTA 0, the launch's row-tile count (ctl[0]) and widest tile (ctl[1]). The CTA then writes its
+// expert's row tiles (expert, first row, rows <= CHUNK_NT), and for each of its tokens, in token order, the token
+// of the sorted row (tok_of) and the sorted row of the (token, slot) pair (slot_of). Tokens of an expert keep
+// their order; the result is the same whatever the grid.
+constexpr int BUCKET_THREADS = 256;
 __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t* __restrict__ masks, int E, int TW,
                                                                  int T, int K, const int32_t* __restrict__ ids,
                                                                  int32_t* __restrict__ slot_of,
                                                                  int32_t* __restrict__ tok_of,
                                                                  int4* __restrict__ groups,
-                                                                 int32_t* __restrict__ ctl, int use_table) {
-  extern __shared__ int pre[];   // [E][TW] when use_table
-  __shared__ int cnt[512], off[512], goff[512], wsum[32], wgsum[32], wmax[32];
+                                                                 int32_t* __restrict__ ctl) {
+  __shared__ int red[4][BUCKET_THREADS / 32];
+  __shared__ int wpre[BUCKET_THREADS / 32];
   pdl_wait();
   pdl_release();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NW = blockDim.x >> 5;
-  // counts (thread = expert) and the prefix table
-  int c = 0;
-  if (tid < E) {
-    const uint32_t* m = masks + (size_t)tid * TW;
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = BUCKET_THREADS / 32;
+  // every expert's count: the experts before e (rows and tiles), the totals
+  int before = 0, gbefore = 0, gtot = 0, wide = 0;
+  for (int x = tid; x < E; x += BUCKET_THREADS) {
+    const uint32_t* m = masks + (size_t)x * TW;
+    int c = 0;
 #pragma unroll 8
-    for (int q = 0; q < TW; ++q) {
-      if (use_table) pre[tid * TW + q] = c;
-      c += __popc(m[q]);
-    }
+    for (int q = 0; q < TW; ++q) c += __popc(__ldcg(m + q));
+    const int ng = (c + CHUNK_NT - 1) / CHUNK_NT;
+    if (x < e) { before += c; gbefore += ng; }
+    gtot += ng;
+    wide = max(wide, min(c, CHUNK_NT));
   }
-  const int ng = (c + CHUNK_NT - 1) / CHUNK_NT;
-  // block-wide exclusive scans of the counts and of the tile counts
-  int v = c, gv = ng;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, v, d), gy = __shfl_up_sync(0xFFFFFFFFu, gv, d);
-    if (lane >= d) { v += y; gv += gy; }
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xFFFFFFFFu, before, o);
+    gbefore += __shfl_xor_sync(0xFFFFFFFFu, gbefore, o);
+    gtot += __shfl_xor_sync(0xFFFFFFFFu, gtot, o);
+    wide = max(wide, __shfl_xor_sync(0xFFFFFFFFu, wide, o));
   }
-  if (lane == 31) { wsum[warp] = v; wgsum[warp] = gv; }
+  if (lane == 0) { red[0][warp] = before; red[1][warp] = gbefore; red[2][warp] = gtot; red[3][warp] = wide; }
   __syncthreads();
-  if (warp == 0) {
-    int sv = lane < NW ? wsum[lane] : 0, sg = lane < NW ? wgsum[lane] : 0;
+  int off = 0, goff = 0;
+  {
+    int gt = 0, wd = 0;
+    for (int w = 0; w < NW; ++w) { off += red[0][w]; goff += red[1][w]; gt += red[2][w]; wd = max(wd, red[3][w]); }
+    if (e == 0 && tid == 0) { ctl[0] = gt; ctl[1] = wd; }
+  }
+  // this expert's tokens: words of its mask in passes of BUCKET_THREADS / 4 words, four threads a word (8 bits
+  // each); a block-wide scan of the words' counts gives each token's rank
+  const uint32_t* m = masks + (size_t)e * TW;
+  int carry = 0;   // tokens of the expert in earlier passes
+  for (int w0 = 0; w0 < TW; w0 += BUCKET_THREADS / 4) {
+    const int q = w0 + (tid >> 2), sub = tid & 3;
+    const uint32_t word = q < TW ? __ldcg(m + q) : 0u;
+    const uint32_t bits = (word >> (8 * sub)) & 0xFFu;
+    // inclusive scan of the per-thread counts over the block (thread order = token order)
+    int v = __popc(bits), incl = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, sv, d), gy = __shfl_up_sync(0xFFFFFFFFu, sg, d);
-      if (lane >= d) { sv += y; sg += gy; }
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= d) incl += y;
     }
-    if (lane < NW) { wsum[lane] = sv; wgsum[lane] = sg; }   // inclusive over warps
-  }
-  __syncthreads();
-  if (tid < E) {
-    cnt[tid] = c;
-    off[tid] = (warp > 0 ? wsum[warp - 1] : 0) + v - c;
-    goff[tid] = (warp > 0 ? wgsum[warp - 1] : 0) + gv - ng;
-  }
-  if (tid == 0) ctl[0] = wgsum[NW - 1];
-  // rows of the widest row tile
-  int wide = __reduce_max_sync(0xFFFFFFFFu, min(c, CHUNK_NT));
-  if (lane == 0) wmax[warp] = wide;
-  __syncthreads();
-  if (warp == 0) {
-    wide = __reduce_max_sync(0xFFFFFFFFu, lane < NW ? wmax[lane] : 0);
-    if (lane == 0) ctl[1] = wide;
-  }
-  for (int e = tid; e < E; e += blockDim.x)
-    for (int g = 0; g * CHUNK_NT < cnt[e]; ++g)
-      groups[goff[e] + g] = make_int4(e, off[e] + g * CHUNK_NT, min(CHUNK_NT, cnt[e] - g * CHUNK_NT), 0);
-  // the (token, slot) pairs, four a thread at a time: the four ids, then the four mask words, are loaded before
-  // any is used (each pass is two dependent global loads, not eight)
-  const int TKp = T * K;
-  for (int p0 = tid; p0 < TKp; p0 += 4 * blockDim.x) {
-    int e[4];
-    uint32_t mw[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int p = p0 + u * blockDim.x;
-      e[u] = p < TKp ? ids[p] : 0;
+    if (lane == 31) wpre[warp] = incl;
+    __syncthreads();
+    int wbase = 0, ptot = 0;
+    for (int w = 0; w < NW; ++w) { wbase += w < warp ? wpre[w] : 0; ptot += wpre[w]; }
+    int rank = carry + wbase + incl - v;
+    for (uint32_t r = bits; r != 0u; r &= r - 1u) {
+      const int t = 32 * q + 8 * sub + (__ffs(r) - 1);
+      const int row = off + rank++;
+      tok_of[row] = t;
+      for (int j = 0; j < K; ++j)
+        if (ids[(size_t)t * K + j] == e) slot_of[(size_t)t * K + j] = row;
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int p = p0 + u * blockDim.x;
-      mw[u] = p < TKp ? masks[(size_t)e[u] * TW + ((p / K) >> 5)] : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int p = p0 + u * blockDim.x;
-      if (p < TKp) {
-        const int t = p / K;
-        int rank = 0;
-        if (use_table) {
-          rank = pre[e[u] * TW + (t >> 5)];
-        } else {
-          const uint32_t* m = masks + (size_t)e[u] * TW;
-          for (int q = 0; q < (t >> 5); ++q) rank += __popc(m[q]);
-        }
-        rank += __popc(mw[u] & ((1u << (t & 31)) - 1u));
-        const int row = off[e[u]] + rank;
-        slot_of[p] = row;
-        tok_of[row] = t;
-      }
-    }
+    carry += ptot;
+    __syncthreads();   // wpre is rewritten by the next pass
   }
+  // the expert's row tiles
+  for (int g = tid; g * CHUNK_NT < carry; g += BUCKET_THREADS)
+    groups[goff + g] = make_int4(e, off + g * CHUNK_NT, min(CHUNK_NT, carry - g * CHUNK_NT), 0);
 }
 
 // xs[row] = xp[tok_of[row]] (fp16 rows of H) and its group sums; one warp per row
@@ -582,11 +561,8 @@ cudaError_t chunk_forward(const MoeLayout& L, const GemmLayout& G, const ChunkSc
     if (e != cudaSuccess) return e;
   }
   ++n;
-  // the prefix table fits in shared memory for chunks up to tens of thousands of tokens
-  const size_t tbl = (size_t)E * TW * sizeof(int);
-  const int use_table = tbl <= BUCKET_TABLE_MAX ? 1 : 0;
-  e = launch_pdl(k_chunk_bucket, 1, BUCKET_THREADS, use_table ? tbl : 0, st, (const uint32_t*)S.masks, E, TW, T, K,
-                 (const int32_t*)S.ids, S.slot_of, S.tok_of, S.groups, S.ctl, use_table);
+  e = launch_pdl(k_chunk_bucket, E, BUCKET_THREADS, 0, st, (const uint32_t*)S.masks, E, TW, T, K,
+                 (const int32_t*)S.ids, S.slot_of, S.tok_of, S.groups, S.ctl);
   if (e != cudaSuccess) return e;
   ++n;
   e = launch_pdl(k_chunk_gather, (T * K + 7) / 8, 256, 0, st, (const uint16_t*)S.xp, (const uint16_t*)S.gs_xp,
