@@ -128,7 +128,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
   const int SPI = (SS / (int)L.SU) & ~1;          // shared units per item (even)
   const int UPI = (SS / (int)L.EU) & ~1;          // expert units per item (even)
   const int SDPI = SS / (int)L.SDR;               // shared-down rows per item
-  const int DRPI = SS / (int)L.DR;                // routed-down rows per item
+  const int DRPI = SS / (int)L.DR;                // routed-down rows per stage
+  // routed-down rows of EPI experts share a stage (expert j of the stage at row j * nrow); a warp reads eight
+  // rows from the middle of an expert's rows on, so the last expert's reads must stay inside the stage
+  const int EPI = nrow > 0 ? max(1, (DRPI - (nrow + 1) / 2 - 8) / nrow + 1) : 1;
 
   if (threadIdx.x == 0) {
 #pragma unroll 1
@@ -197,12 +200,25 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
         for (int u = u0; ok && u < u1; u += UPI)
           ok = issue(gu + (size_t)u * L.EU, (uint32_t)(min(UPI, u1 - u) * L.EU));
       }
+      // the routed down rows, EPI experts a stage: one expect-tx for the stage, one copy per expert
 #pragma unroll 1
-      for (int aa = 0; ok && aa < U; ++aa) {
-        const uint8_t* dn = a.ex_dn + (size_t)ctl->act_e[aa] * L.exdn_expert + (size_t)r0 * L.DR;
+      for (int aa0 = 0; ok && aa0 < U && nrow > 0; aa0 += EPI) {
+        const int ne = min(EPI, U - aa0);
+        const uint32_t eb = (uint32_t)(nrow * L.DR);
+        if (ctl->abort) { ok = false; break; }
+        if (n >= NS && !mbar_wait(&ctl->empty[ps], pph ^ 1u, a.timeout_ns)) {
+          set_error(a, ctl, ERR_WAIT_EMPTY);
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&ctl->full[ps], eb * (uint32_t)ne);
 #pragma unroll 1
-        for (int rr = 0; ok && rr < nrow; rr += DRPI)
-          ok = issue(dn + (size_t)rr * L.DR, (uint32_t)(min(DRPI, nrow - rr) * L.DR));
+        for (int j = 0; j < ne; ++j)
+          bulk_g2s_hint(ring + (size_t)ps * SS + (size_t)j * eb,
+                        a.ex_dn + (size_t)ctl->act_e[aa0 + j] * L.exdn_expert + (size_t)r0 * L.DR, eb,
+                        &ctl->full[ps], pol);
+        ++n;
+        if (++ps == NS) { ps = 0; pph ^= 1u; }
       }
       stamp(a, 18);
       // drain: every issued copy must have landed before the CTA may leave
@@ -619,11 +635,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       constexpr int PC = 2;
       const int half = (nrow + 1) / 2;
       int ui = 0;
+      const uint8_t* stage = nullptr;
 #pragma unroll 1
-      for (int aa = 0; aa < U; ++aa) {
+      for (int aa = 0; aa < U && nrow > 0; ++aa) {
         const int pb = ctl->act_pb[aa], na = (int)ctl->act_pb[aa + 1] - pb;
         const int nunits = 2 * ((na + PC - 1) / PC);
-        const uint8_t* item = acquire();
+        if (aa % EPI == 0) stage = acquire();
+        const uint8_t* item = stage + (size_t)(aa % EPI) * nrow * L.DR;
 #pragma unroll 1
         for (int k = 0; k < nunits; ++k, ++ui) {
           if (ui % NCW != cw || warp_abort(ctl)) continue;
@@ -671,7 +689,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
             if ((lane & 3) == 0 && pp < np && rlo + idx < rhi) yv[(size_t)(p0 + pp) * nrow + rlo + idx] = z;
           }
         }
-        release();
+        if (aa % EPI == EPI - 1 || aa == U - 1) release();
       }
     }
     named_bar(BAR_C, CT);
