@@ -217,7 +217,9 @@ static_assert(sizeof(Bars) <= S_BYTES - S_BAR, "barrier area");
 
 // debug stamps (CTA 0, first 64 K-tiles): events 0 producer issued, 1 dequant saw the stage, 2 dequant done,
 // 3 MMA issued, 4 epilogue saw the accumulator (at the job's last K-tile), 5 epilogue read it, 6 MMA saw A ready
-#define GSTAMP(ev, k) do { if (g.trace && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
+// (only the traced instantiation of the kernel, TR = true, carries them: every instruction of the MMA warp's
+// per-K-tile loop is on the pipeline's critical path)
+#define GSTAMP(ev, k) do { if (TR && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
 
 __device__ __forceinline__ float silu_c(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
@@ -238,6 +240,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // rows of a TMA box for a job of N rows (boxes of 16, 32 or 64)
 __device__ __forceinline__ int box_of(int n) { return n <= 16 ? 0 : n <= 32 ? 1 : 2; }
 
+template <bool TR>
 __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -384,6 +387,12 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     job_begin(g, ngroups, tw, it);
     Job jb;
     SlotRing sl, sr;
+    // B descriptors of stage 0 and of bias tile 0; a stage (bias tile) further on adds its byte offset / 16 to
+    // the start-address field (shared-memory addresses stay below 256 KB, so the field never carries)
+    const uint64_t dh0 = umma_desc_sw128(smem_u32(smem + geo.bhi)), dl0 = umma_desc_sw128(smem_u32(smem + geo.blo));
+    const uint64_t db0 = umma_desc_sw128(smem_u32(smem + S_BB));
+    const uint32_t sstep = (uint32_t)geo.bytes >> 4;
+    const uint32_t dh_lo = (uint32_t)dh0, dh_hi = (uint32_t)(dh0 >> 32), dl_lo = (uint32_t)dl0, dl_hi = (uint32_t)(dl0 >> 32);
     while (run && job_next(g, it, jb)) {
       const uint32_t idesc = umma_idesc_f16(128, jb.n);
       const bool lo = jb.lomap >= 0;
@@ -402,34 +411,25 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
         tc_fence_after();
         // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
-        const uint8_t* st = smem + s * geo.bytes;
-        const uint64_t bh = umma_desc_sw128(smem_u32(st + geo.bhi)), bl = umma_desc_sw128(smem_u32(st + geo.blo));
-        const uint64_t bb = umma_desc_sw128(smem_u32(smem + S_BB + pb * BB_BYTES));
+        const uint32_t so = (uint32_t)s * sstep;
         const uint32_t a = tmem + a0 + 64u * (uint32_t)t;
         if (elect_one()) {
           GSTAMP(6, gk);
-          // D += A1 B + A2 B: the exact products s q x
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
-            umma_f16_ts(d, a + 32 + 8 * ks, bh + 2 * ks, idesc, 1u);
-          }
-          if (lo)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_f16_ts(d + tlo, a + 8 * ks, bl + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
+          // D += A1 B + A2 B: the exact products s q x; then the low halves' D_lo += A1 B_lo
+          umma_f16_ktile<true>(d, a, dh_lo + so, dh_hi, idesc, kt > 0 ? 1u : 0u);
+          if (lo) umma_f16_ktile<false>(d + tlo, a, dl_lo + so, dl_hi, idesc, kt > 0 ? 1u : 0u);
           umma_commit(&bar->empty[s]);
           umma_commit(&bar->a_free[t]);
           if (last) {
             // the offset term: D += (b_g, b_g) . (sum_hi_g, sum_lo_g) over the job's groups, 8 groups per
             // K step; the bias columns past the job's groups are zero
             const int nbk = (jb.ktiles + 7) >> 3, kb0 = jb.k0 >> 3;   // k0: a multiple of 8 groups
+            const uint64_t bb = db0 + (uint64_t)(pb * (BB_BYTES >> 4));
             for (int ks = 0; ks < nbk; ++ks) umma_f16_ts(d, ab + 8 * ks, bb + 2 * (kb0 + ks), idesc, 1u);
             umma_commit(&bar->acc_full[pb]);
           }
           GSTAMP(3, gk);
         }
-        __syncwarp();
       }
       ++njob;
     }
@@ -659,7 +659,9 @@ cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
   {
     std::lock_guard<std::mutex> lk(g_gemm_attr_mutex);
     if (!configured[dev]) {
-      e = cudaFuncSetAttribute(k_chunk_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+      e = cudaFuncSetAttribute(k_chunk_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_chunk_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
       if (e != cudaSuccess) return e;
       configured[dev] = true;
     }
@@ -675,7 +677,7 @@ cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_chunk_gemm, g);
+  return g.trace ? cudaLaunchKernelEx(&cfg, k_chunk_gemm<true>, g) : cudaLaunchKernelEx(&cfg, k_chunk_gemm<false>, g);
 }
 
 }  // namespace moe
