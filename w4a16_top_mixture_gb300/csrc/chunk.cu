@@ -16,7 +16,10 @@ static size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 // Every kernel of the chunk path is launched programmatic-dependent: its CTAs may become resident while the
 // previous kernel on the stream still runs (once every CTA of that one has run launch_dependents or exited), and
 // each kernel runs griddepcontrol.wait before it reads anything an earlier kernel writes, or writes anything an
-// earlier kernel reads. Only launch latency and set-up overlap; no data is read early.
+// earlier kernel reads. Only launch latency and set-up overlap; no data is read early. Data an earlier kernel
+// wrote is read through L2 (ld.global.cg): with launches overlapping, a line of it that an earlier launch left
+// in this SM's L1 can be stale (the GEMM's tile list read that way computed a wrong job about once in a few
+// hundred chunk forwards of alternating sizes).
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_pdl(void (*k)(KArgs...), int grid, int block, size_t smem, cudaStream_t st,
                               Args&&... args) {
@@ -251,7 +254,7 @@ k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
       float ss = 0.f;
 #pragma unroll 8
       for (int i = lane; i < H; i += 32) {
-        const float v = __half2float(__ushort_as_half(xr[i]));
+        const float v = __half2float(__ushort_as_half(__ldcg(xr + i)));
         ss += v * v;
       }
       ss = warp_sum_c(ss);
@@ -266,7 +269,7 @@ k_chunk_prologue(const uint16_t* __restrict__ x, const uint16_t* __restrict__ ga
   for (int base = part * 32; base < nblk; base += 32 * PRO_WPT) {
     const int blk = base + lane;
     const bool on = blk < nblk;   // the same for the eight lanes of a group
-    const uint4 raw = on ? *reinterpret_cast<const uint4*>(xr + blk * 8) : make_uint4(0, 0, 0, 0);
+    const uint4 raw = on ? __ldcg(reinterpret_cast<const uint4*>(xr + blk * 8)) : make_uint4(0, 0, 0, 0);
     const uint4 graw = (gamma && on) ? *reinterpret_cast<const uint4*>(gamma + blk * 8) : make_uint4(0, 0, 0, 0);
     const uint16_t* h8 = reinterpret_cast<const uint16_t*>(&raw);
     const uint16_t* g8 = reinterpret_cast<const uint16_t*>(&graw);
@@ -376,7 +379,7 @@ __global__ void k_chunk_route(const float* __restrict__ logits, int np, int E, i
 // of the sorted row (tok_of) and the sorted row of the (token, slot) pair (slot_of). Tokens of an expert keep
 // their order; the result is the same whatever the grid.
 constexpr int BUCKET_THREADS = 256;
-__global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t* __restrict__ masks, int E, int TW,
+__global__ void __launch_bounds__(BUCKET_THREADS, 1) k_chunk_bucket(const uint32_t* __restrict__ masks, int E, int TW,
                                                                  int T, int K, const int32_t* __restrict__ ids,
                                                                  int32_t* __restrict__ slot_of,
                                                                  int32_t* __restrict__ tok_of,
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(BUCKET_THREADS) k_chunk_bucket(const uint32_t*
       const int row = off + rank++;
       tok_of[row] = t;
       for (int j = 0; j < K; ++j)
-        if (ids[(size_t)t * K + j] == e) slot_of[(size_t)t * K + j] = row;
+        if (__ldcg(ids + (size_t)t * K + j) == e) slot_of[(size_t)t * K + j] = row;
     }
     carry += ptot;
     __syncthreads();   // wpre is rewritten by the next pass
@@ -458,7 +461,7 @@ __global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const uint16_t* 
   pdl_release();
   const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x & 31;
   if (r >= rows) return;
-  const int t = tok_of[r];
+  const int t = __ldcg(tok_of + r);
   const uint4* src = reinterpret_cast<const uint4*>(xp + (size_t)t * H);
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)r * H);
   // eight 16-byte loads a lane in flight before the stores
@@ -467,7 +470,7 @@ __global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const uint16_t* 
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int i = b0 + k * 32 + lane;
-      v[k] = i < H / 8 ? src[i] : make_uint4(0, 0, 0, 0);
+      v[k] = i < H / 8 ? __ldcg(src + i) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -478,7 +481,7 @@ __global__ void k_chunk_gather(const uint16_t* __restrict__ xp, const uint16_t* 
   // the 128-byte group-sum row: 8 lanes of 16 bytes
   if (lane < GSUM_COLS / 8)
     reinterpret_cast<uint4*>(gs_xs + (size_t)r * GSUM_COLS)[lane] =
-        reinterpret_cast<const uint4*>(gs_xp + (size_t)t * GSUM_COLS)[lane];
+        __ldcg(reinterpret_cast<const uint4*>(gs_xp + (size_t)t * GSUM_COLS) + lane);
 }
 
 // out[t][r] = sum_j w[t][j] * y[slot(t, j)][r] + sg[t] * ys[t][r] (+ h[t][r]), rounded to fp16 once. A thread
@@ -501,14 +504,14 @@ __global__ void k_chunk_combine(const float* __restrict__ y, const float* __rest
 #pragma unroll
     for (int j = 0; j < KM; ++j)
       if (j < K) {
-        sl[j] = slot_of[(size_t)t * K + j];
-        wv[j] = w[(size_t)t * K + j];
+        sl[j] = __ldcg(slot_of + (size_t)t * K + j);
+        wv[j] = __ldcg(w + (size_t)t * K + j);
       }
     float4 yv[KM];
 #pragma unroll
     for (int j = 0; j < KM; ++j)
-      if (j < K) yv[j] = *reinterpret_cast<const float4*>(y + (size_t)sl[j] * H + c);
-    const float4 sv = *reinterpret_cast<const float4*>(ys + (size_t)t * H + c);
+      if (j < K) yv[j] = __ldcg(reinterpret_cast<const float4*>(y + (size_t)sl[j] * H + c));
+    const float4 sv = __ldcg(reinterpret_cast<const float4*>(ys + (size_t)t * H + c));
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
     for (int j = 0; j < KM; ++j)
@@ -518,13 +521,13 @@ __global__ void k_chunk_combine(const float* __restrict__ y, const float* __rest
         a2 += wv[j] * yv[j].z;
         a3 += wv[j] * yv[j].w;
       }
-    const float g = sg[t];
+    const float g = __ldcg(sg + t);
     a0 += g * sv.x;
     a1 += g * sv.y;
     a2 += g * sv.z;
     a3 += g * sv.w;
     if (resid) {
-      const uint2 rr = *reinterpret_cast<const uint2*>(resid + (size_t)t * H + c);
+      const uint2 rr = __ldcg(reinterpret_cast<const uint2*>(resid + (size_t)t * H + c));
       a0 += __half2float(__ushort_as_half((uint16_t)(rr.x & 0xFFFFu)));
       a1 += __half2float(__ushort_as_half((uint16_t)(rr.x >> 16)));
       a2 += __half2float(__ushort_as_half((uint16_t)(rr.y & 0xFFFFu)));

@@ -190,7 +190,7 @@ struct JobIter {
 __device__ __forceinline__ int4 job_group(const GemmArgs& g, int ngroups, int j) {
   const int MT = g.phase == 2 ? 2 * g.G.I / 128 : g.G.H / 128;
   if (g.phase == 1 || ngroups <= 0 || j >= MT * ngroups) return make_int4(0, 0, 0, 0);
-  return g.S.groups[j % ngroups];
+  return __ldcg(g.S.groups + (j % ngroups));
 }
 __device__ __forceinline__ void job_begin(const GemmArgs& g, int ngroups, int tw, JobIter& it) {
   it.j = blockIdx.x;
@@ -217,9 +217,7 @@ static_assert(sizeof(Bars) <= S_BYTES - S_BAR, "barrier area");
 
 // debug stamps (CTA 0, first 64 K-tiles): events 0 producer issued, 1 dequant saw the stage, 2 dequant done,
 // 3 MMA issued, 4 epilogue saw the accumulator (at the job's last K-tile), 5 epilogue read it, 6 MMA saw A ready
-// (only the traced instantiation of the kernel, TR = true, carries them: every instruction of the MMA warp's
-// per-K-tile loop is on the pipeline's critical path)
-#define GSTAMP(ev, k) do { if (TR && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
+#define GSTAMP(ev, k) do { if (g.trace && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
 
 __device__ __forceinline__ float silu_c(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
@@ -240,7 +238,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // rows of a TMA box for a job of N rows (boxes of 16, 32 or 64)
 __device__ __forceinline__ int box_of(int n) { return n <= 16 ? 0 : n <= 32 ? 1 : 2; }
 
-template <bool TR>
 __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -284,8 +281,8 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
   if (tid == 0) {
     // phase 1 tiles the tokens 64 at a time; phases 2 and 3 take the bucketing's row tiles, and phase 3 tiles
     // the shared down's tokens as wide as the widest row tile, so no job is wider than that
-    bar->ngroups = g.phase == 1 ? 0 : g.S.ctl[0];
-    bar->tw = g.phase == 1 ? CHUNK_NT : min(CHUNK_NT, max(16, (g.S.ctl[1] + 15) & ~15));
+    bar->ngroups = g.phase == 1 ? 0 : __ldcg(g.S.ctl);
+    bar->tw = g.phase == 1 ? CHUNK_NT : min(CHUNK_NT, max(16, (__ldcg(g.S.ctl + 1) + 15) & ~15));
     fence_mbar_init();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
@@ -392,7 +389,6 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     const uint64_t dh0 = umma_desc_sw128(smem_u32(smem + geo.bhi)), dl0 = umma_desc_sw128(smem_u32(smem + geo.blo));
     const uint64_t db0 = umma_desc_sw128(smem_u32(smem + S_BB));
     const uint32_t sstep = (uint32_t)geo.bytes >> 4;
-    const uint32_t dh_lo = (uint32_t)dh0, dh_hi = (uint32_t)(dh0 >> 32), dl_lo = (uint32_t)dl0, dl_hi = (uint32_t)(dl0 >> 32);
     while (run && job_next(g, it, jb)) {
       const uint32_t idesc = umma_idesc_f16(128, jb.n);
       const bool lo = jb.lomap >= 0;
@@ -411,13 +407,20 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
         tc_fence_after();
         // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
-        const uint32_t so = (uint32_t)s * sstep;
+        const uint64_t so = (uint64_t)((uint32_t)s * sstep);
+        const uint64_t bh = dh0 + so, bl = dl0 + so;
         const uint32_t a = tmem + a0 + 64u * (uint32_t)t;
         if (elect_one()) {
-          GSTAMP(6, gk);
-          // D += A1 B + A2 B: the exact products s q x; then the low halves' D_lo += A1 B_lo
-          umma_f16_ktile<true>(d, a, dh_lo + so, dh_hi, idesc, kt > 0 ? 1u : 0u);
-          if (lo) umma_f16_ktile<false>(d + tlo, a, dl_lo + so, dl_hi, idesc, kt > 0 ? 1u : 0u);
+          // D += A1 B + A2 B: the exact products s q x
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
+            umma_f16_ts(d, a + 32 + 8 * ks, bh + 2 * ks, idesc, 1u);
+          }
+          if (lo)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              umma_f16_ts(d + tlo, a + 8 * ks, bl + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&bar->empty[s]);
           umma_commit(&bar->a_free[t]);
           if (last) {
@@ -428,8 +431,8 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
             for (int ks = 0; ks < nbk; ++ks) umma_f16_ts(d, ab + 8 * ks, bb + 2 * (kb0 + ks), idesc, 1u);
             umma_commit(&bar->acc_full[pb]);
           }
-          GSTAMP(3, gk);
         }
+        __syncwarp();
       }
       ++njob;
     }
@@ -570,11 +573,11 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
       for (int c0 = 0; c0 < jb.n; c0 += 16) {
         uint32_t v[16];
         tmem_ld16_nowait(d + c0, v);
-        tmem_wait_ld();
+        tmem_wait_ld(v);
         if (jb.lomap >= 0) {
           uint32_t w[16];
           tmem_ld16_nowait(d + tlo + c0, w);
-          tmem_wait_ld();
+          tmem_wait_ld(w);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             ep[r * 65 + c0 + i] = fmaf(__uint_as_float(w[i]), 1.0f / 4096.0f, __uint_as_float(v[i]));
@@ -659,9 +662,7 @@ cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
   {
     std::lock_guard<std::mutex> lk(g_gemm_attr_mutex);
     if (!configured[dev]) {
-      e = cudaFuncSetAttribute(k_chunk_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_chunk_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+      e = cudaFuncSetAttribute(k_chunk_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
       if (e != cudaSuccess) return e;
       configured[dev] = true;
     }
@@ -677,7 +678,7 @@ cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return g.trace ? cudaLaunchKernelEx(&cfg, k_chunk_gemm<true>, g) : cudaLaunchKernelEx(&cfg, k_chunk_gemm<false>, g);
+  return cudaLaunchKernelEx(&cfg, k_chunk_gemm, g);
 }
 
 }  // namespace moe

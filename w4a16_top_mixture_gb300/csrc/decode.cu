@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
         float ss = 0.f;
 #pragma unroll 1
         for (int i = lane * 8; i < H; i += 256) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(xr + i);
+          const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(xr + i));
           const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
       const int i = base + lane, t = i / (NCH * 4), c = (i >> 2) % NCH, j = i & 3;
       const bool live = i < T * NCH * 4;
       float v[8];
-      const uint4 raw = live ? *reinterpret_cast<const uint4*>(a.x + (size_t)t * H + c * 32 + j * 8) : make_uint4(0, 0, 0, 0);
+      const uint4 raw = live ? __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H + c * 32 + j * 8)) : make_uint4(0, 0, 0, 0);
       const __half* h8 = reinterpret_cast<const __half*>(&raw);
       if (a.gamma) {
         const float rn = live ? ctl->rn[t] : 0.f;
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) k_decode(DecodeArgs a, int NS,
 #pragma unroll 1
         for (int j = 0; j < K; ++j) acc += ctl->wts[t][j] * yv[(size_t)ctl->tok_pair[t][j] * nrow + rr];
         float v = acc + ctl->sg[t] * shs[t * nrow + rr];
-        if (a.gamma) v += __half2float(__ushort_as_half(a.x[(size_t)t * H + r0 + rr]));
+        if (a.gamma) v += __half2float(__ushort_as_half(__ldcg(a.x + (size_t)t * H + r0 + rr)));
         const uint16_t o = __half_as_ushort(__float2half_rn(v));
         a.out[(size_t)t * H + r0 + rr] = o;
         if (a.out2) a.out2[(size_t)t * H + r0 + rr] = o;

@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
         float ss = 0.f;
 #pragma unroll 1
         for (int i = lane * 8; i < H; i += 256) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(a.x + i);
+          const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(a.x + i));
           const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
       const int i = base + lane, c = i >> 2, j = i & 3;
       const bool live = i < NCH * 4;
       float v[8];
-      const uint4 raw = live ? *reinterpret_cast<const uint4*>(a.x + c * 32 + j * 8) : make_uint4(0, 0, 0, 0);
+      const uint4 raw = live ? __ldcg(reinterpret_cast<const uint4*>(a.x + c * 32 + j * 8)) : make_uint4(0, 0, 0, 0);
       const __half* h8 = reinterpret_cast<const __half*>(&raw);
       if (a.gamma) {
         const uint4 graw = live ? *reinterpret_cast<const uint4*>(a.gamma + c * 32 + j * 8) : make_uint4(0, 0, 0, 0);
@@ -672,7 +672,7 @@ __global__ void __launch_bounds__(DEC1_THREADS, 2) k_decode1(DecodeArgs a) {
 #pragma unroll
         for (int j = 0; j < K; ++j) acc += ctl->wts[j] * yv[j * rows_max + rr];
         float v = acc + ctl->sg * shs[rr];
-        if (a.gamma) v += __half2float(__ushort_as_half(a.x[r0 + rr]));
+        if (a.gamma) v += __half2float(__ushort_as_half(__ldcg(a.x + r0 + rr)));
         const uint16_t o = __half_as_ushort(__float2half_rn(v));
         a.out[r0 + rr] = o;
         if (a.out2) a.out2[r0 + rr] = o;
