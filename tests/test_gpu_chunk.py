@@ -135,6 +135,33 @@ def test_chunk_split_is_byte_equal():
     blk.close()
 
 
+def test_chunk_alternating_sizes_are_byte_equal():
+    """Chunk forwards of two sizes alternating on one handle give the same bytes every time. (When the GEMM read
+    the bucketing's tile list through L1, a line left there by an earlier launch could be stale under the
+    overlapping launches, and about one forward in a few hundred computed a CTA's first job from the wrong tile
+    when the size changed between calls.)"""
+    import torch
+    build.build()
+    cfg = synth.PROD
+    w, x = make_case(cfg, 512, 90)
+    blk = lib.MoeBlock.from_config(cfg, max_tokens=512)
+    blk.load_weights(lib.upload_weights(w))
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
+    xa = xd[:256].contiguous()
+    ref_w = ref_a = None
+    for _ in range(60):
+        o_w = blk.forward(xd).cpu().numpy().view(np.uint16)
+        o_a = blk.forward(xa).cpu().numpy().view(np.uint16)
+        if ref_w is None:
+            ref_w, ref_a = o_w.copy(), o_a.copy()
+            np.testing.assert_array_equal(ref_w[:256], ref_a)
+        np.testing.assert_array_equal(o_w, ref_w)
+        np.testing.assert_array_equal(o_a, ref_a)
+    torch.cuda.synchronize()
+    assert blk.status()[0] == 0
+    blk.close()
+
+
 @pytest.mark.parametrize("T", [517, 600])
 def test_chunk_repeats_are_byte_equal(T):
     """The same chunk forwarded again and again on one handle gives the same bytes every time: the GEMM's
