@@ -41,6 +41,10 @@
 //                  bias A of parity p are final and read                      (MMA commit -> epilogue, producer,
 //                                                                              dequantisation)
 //   acc_free[p]    the epilogue has read the accumulator of parity p          (epilogue -> MMA)
+// A wait on a phase parity passes at once if the barrier is still one phase behind (its previous phase has the
+// other parity), so no role may wait for a barrier's use u + 1 while its use u can still be pending. The three
+// dequantisation groups step through the stages independently, so a group first waits for a stage's previous
+// release (empty) before its fill (full). Every other barrier is waited on in the order of its uses.
 // Every wait is bounded; on a timeout the CTA records an error bit and every role leaves its loops.
 #include <mutex>
 #include <cuda_fp16.h>
@@ -217,7 +221,9 @@ static_assert(sizeof(Bars) <= S_BYTES - S_BAR, "barrier area");
 
 // debug stamps (CTA 0, first 64 K-tiles): events 0 producer issued, 1 dequant saw the stage, 2 dequant done,
 // 3 MMA issued, 4 epilogue saw the accumulator (at the job's last K-tile), 5 epilogue read it, 6 MMA saw A ready
-#define GSTAMP(ev, k) do { if (g.trace && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
+// (only the traced instantiation of the kernel, TR = true, carries them: every instruction of the MMA warp's
+// per-K-tile loop is on the pipeline's critical path)
+#define GSTAMP(ev, k) do { if (TR && blockIdx.x == 0 && (k) < 64) g.trace[(ev) * 64 + (k)] = clock64(); } while (0)
 
 __device__ __forceinline__ float silu_c(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
@@ -238,6 +244,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // rows of a TMA box for a job of N rows (boxes of 16, 32 or 64)
 __device__ __forceinline__ int box_of(int n) { return n <= 16 ? 0 : n <= 32 ? 1 : 2; }
 
+template <bool TR>
 __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -389,6 +396,7 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
     const uint64_t dh0 = umma_desc_sw128(smem_u32(smem + geo.bhi)), dl0 = umma_desc_sw128(smem_u32(smem + geo.blo));
     const uint64_t db0 = umma_desc_sw128(smem_u32(smem + S_BB));
     const uint32_t sstep = (uint32_t)geo.bytes >> 4;
+    const uint32_t dh_lo = (uint32_t)dh0, dh_hi = (uint32_t)(dh0 >> 32), dl_lo = (uint32_t)dl0, dl_hi = (uint32_t)(dl0 >> 32);
     while (run && job_next(g, it, jb)) {
       const uint32_t idesc = umma_idesc_f16(128, jb.n);
       const bool lo = jb.lomap >= 0;
@@ -398,31 +406,35 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         const bool ok = njob < 2 || wait(&bar->acc_free[pb], ((njob >> 1) - 1) & 1u);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
       }
-      for (int kt = 0; kt < jb.ktiles; ++kt, ++gk, sl.next(nt), sr.next(NSG)) {
-        const int s = sr.t, t = sl.t;
+      // two K-tiles per pass where the job has them: one vote and one fence for both
+      for (int kt = 0; kt < jb.ktiles;) {
+        const int n2 = kt + 1 < jb.ktiles ? 2 : 1;
+        SlotRing sl1 = sl, sr1 = sr;
+        sl1.next(nt);
+        sr1.next(NSG);
         // a_ready implies full[s] (the dequantisation waited for it)
-        bool ok = wait(&bar->a_ready[t], sl.ph);
-        const bool last = kt == jb.ktiles - 1;
+        bool ok = wait(&bar->a_ready[sl.t], sl.ph);
+        if (n2 == 2) ok = ok && wait(&bar->a_ready[sl1.t], sl1.ph);
+        const bool last = kt + n2 == jb.ktiles;
         if (last) ok = ok && wait(&bar->bb_full[pb], (njob >> 1) & 1u);
         if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
         tc_fence_after();
-        // B descriptors of the stage; a K step of 16 elements advances the start address by 32 bytes (2 units)
-        const uint64_t so = (uint64_t)((uint32_t)s * sstep);
-        const uint64_t bh = dh0 + so, bl = dl0 + so;
-        const uint32_t a = tmem + a0 + 64u * (uint32_t)t;
+        // B descriptors of the stages; a K step of 16 elements advances the start address by 32 bytes (2 units)
+        const uint32_t so0 = (uint32_t)sr.t * sstep, so1 = (uint32_t)sr1.t * sstep;
+        const uint32_t a0t = tmem + a0 + 64u * (uint32_t)sl.t, a1t = tmem + a0 + 64u * (uint32_t)sl1.t;
         if (elect_one()) {
-          // D += A1 B + A2 B: the exact products s q x
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            umma_f16_ts(d, a + 8 * ks, bh + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
-            umma_f16_ts(d, a + 32 + 8 * ks, bh + 2 * ks, idesc, 1u);
+          GSTAMP(6, gk);
+          // D += A1 B + A2 B: the exact products s q x; then the low halves' D_lo += A1 B_lo
+          umma_f16_ktile<true>(d, a0t, dh_lo + so0, dh_hi, idesc, kt > 0 ? 1u : 0u);
+          if (lo) umma_f16_ktile<false>(d + tlo, a0t, dl_lo + so0, dl_hi, idesc, kt > 0 ? 1u : 0u);
+          umma_commit(&bar->empty[sr.t]);
+          umma_commit(&bar->a_free[sl.t]);
+          if (n2 == 2) {
+            umma_f16_ktile<true>(d, a1t, dh_lo + so1, dh_hi, idesc, 1u);
+            if (lo) umma_f16_ktile<false>(d + tlo, a1t, dl_lo + so1, dl_hi, idesc, 1u);
+            umma_commit(&bar->empty[sr1.t]);
+            umma_commit(&bar->a_free[sl1.t]);
           }
-          if (lo)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_f16_ts(d + tlo, a + 8 * ks, bl + 2 * ks, idesc, (kt > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&bar->empty[s]);
-          umma_commit(&bar->a_free[t]);
           if (last) {
             // the offset term: D += (b_g, b_g) . (sum_hi_g, sum_lo_g) over the job's groups, 8 groups per
             // K step; the bias columns past the job's groups are zero
@@ -431,8 +443,16 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
             for (int ks = 0; ks < nbk; ++ks) umma_f16_ts(d, ab + 8 * ks, bb + 2 * (kb0 + ks), idesc, 1u);
             umma_commit(&bar->acc_full[pb]);
           }
+          GSTAMP(3, gk);
         }
-        __syncwarp();
+        if (n2 == 2) {
+          sl = sl1;
+          sr = sr1;
+        }
+        sl.next(nt);
+        sr.next(NSG);
+        gk += (uint32_t)n2;
+        kt += n2;
       }
       ++njob;
     }
@@ -471,7 +491,8 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         const int s = sr.t, t = sl.t;
         // the stage landed; A slot t is free (the MMAs of K-tile gk - nt completed); the bias columns of
         // parity pb are free (the bias MMA of job njob - 2 completed)
-        if (!wait(&bar->full[s], sr.ph) || (gk >= (uint32_t)nt && !wait(&bar->a_free[t], sl.ph ^ 1u)) ||
+        if ((gk >= NSG && !wait(&bar->empty[s], sr.ph ^ 1u)) || !wait(&bar->full[s], sr.ph) ||
+            (gk >= (uint32_t)nt && !wait(&bar->a_free[t], sl.ph ^ 1u)) ||
             (njob >= 2 && !wait(&bar->acc_full[pb], ((njob >> 1) - 1) & 1u)))
           break;
         tc_fence_after();
@@ -662,7 +683,9 @@ cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
   {
     std::lock_guard<std::mutex> lk(g_gemm_attr_mutex);
     if (!configured[dev]) {
-      e = cudaFuncSetAttribute(k_chunk_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+      e = cudaFuncSetAttribute(k_chunk_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_chunk_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
       if (e != cudaSuccess) return e;
       configured[dev] = true;
     }
@@ -678,7 +701,7 @@ cudaError_t chunk_gemm_launch(const GemmArgs& g, int grid, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_chunk_gemm, g);
+  return g.trace ? cudaLaunchKernelEx(&cfg, k_chunk_gemm<true>, g) : cudaLaunchKernelEx(&cfg, k_chunk_gemm<false>, g);
 }
 
 }  // namespace moe

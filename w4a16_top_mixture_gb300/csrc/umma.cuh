@@ -74,6 +74,47 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The MMAs of one K-tile (64 columns) as one issue sequence: for each 16-column K step k, D += A[k] B[k] then
+// D += A[32 + k] B[k], A at TMEM columns a + 8k and a + 32 + 8k, B at descriptor b + 2k (its start address
+// advanced by 32 bytes). The descriptor is passed as its two halves (the start address sits in the low half and
+// never carries into the high one), so the steps need 32-bit adds only; the first MMA accumulates onto D only
+// if acc_first is nonzero. PAIRS = false: the single sequence D += A[k] B[k] (A columns a + 8k).
+template <bool PAIRS>
+__device__ __forceinline__ void umma_f16_ktile(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                               uint32_t idesc, uint32_t acc_first) {
+  if (PAIRS) {
+    asm volatile(
+        "{\n .reg .pred pf, pt;\n .reg .b32 l1, l2, l3, x1, x2, x3, y0, y1, y2, y3;\n .reg .b64 q0, q1, q2, q3;\n"
+        " setp.ne.b32 pf, %5, 0;\n setp.eq.b32 pt, %4, %4;\n"
+        " add.u32 l1, %2, 2;\n add.u32 l2, %2, 4;\n add.u32 l3, %2, 6;\n"
+        " mov.b64 q0, {%2, %3};\n mov.b64 q1, {l1, %3};\n mov.b64 q2, {l2, %3};\n mov.b64 q3, {l3, %3};\n"
+        " add.u32 x1, %1, 8;\n add.u32 x2, %1, 16;\n add.u32 x3, %1, 24;\n"
+        " add.u32 y0, %1, 32;\n add.u32 y1, %1, 40;\n add.u32 y2, %1, 48;\n add.u32 y3, %1, 56;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], q0, %4, pf;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [y0], q0, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], q1, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [y1], q1, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], q2, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [y2], q2, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], q3, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [y3], q3, %4, pt;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc_first)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n .reg .pred pf, pt;\n .reg .b32 l1, l2, l3, x1, x2, x3;\n .reg .b64 q0, q1, q2, q3;\n"
+        " setp.ne.b32 pf, %5, 0;\n setp.eq.b32 pt, %4, %4;\n"
+        " add.u32 l1, %2, 2;\n add.u32 l2, %2, 4;\n add.u32 l3, %2, 6;\n"
+        " mov.b64 q0, {%2, %3};\n mov.b64 q1, {l1, %3};\n mov.b64 q2, {l2, %3};\n mov.b64 q3, {l3, %3};\n"
+        " add.u32 x1, %1, 8;\n add.u32 x2, %1, 16;\n add.u32 x3, %1, 24;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], q0, %4, pf;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], q1, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], q2, %4, pt;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], q3, %4, pt;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(acc_first)
+        : "memory");
+  }
+}
 // mbarrier arrives once all previously issued MMAs of this thread have completed
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
