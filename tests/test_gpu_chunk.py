@@ -136,10 +136,10 @@ def test_chunk_split_is_byte_equal():
 
 
 def test_chunk_alternating_sizes_are_byte_equal():
-    """Chunk forwards of two sizes alternating on one handle give the same bytes every time. (When the GEMM read
-    the bucketing's tile list through L1, a line left there by an earlier launch could be stale under the
-    overlapping launches, and about one forward in a few hundred computed a CTA's first job from the wrong tile
-    when the size changed between calls.)"""
+    """Chunk forwards of two sizes alternating on one handle give the same bytes every time. (While a
+    dequantisation group could wait for a stage's next fill before its previous fill had landed, a barrier-parity
+    false positive, about one forward in a few hundred to a hundred computed a CTA's first down-projection job
+    from a stage whose copy had not landed; start-up timing, which changes with the size, set the rate.)"""
     import torch
     build.build()
     cfg = synth.PROD

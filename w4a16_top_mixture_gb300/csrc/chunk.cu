@@ -17,9 +17,8 @@ static size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
 // previous kernel on the stream still runs (once every CTA of that one has run launch_dependents or exited), and
 // each kernel runs griddepcontrol.wait before it reads anything an earlier kernel writes, or writes anything an
 // earlier kernel reads. Only launch latency and set-up overlap; no data is read early. Data an earlier kernel
-// wrote is read through L2 (ld.global.cg): with launches overlapping, a line of it that an earlier launch left
-// in this SM's L1 can be stale (the GEMM's tile list read that way computed a wrong job about once in a few
-// hundred chunk forwards of alternating sizes).
+// wrote is read through L2 (ld.global.cg): while launches overlap, nothing is taken to keep a line of it that an
+// earlier launch left in this SM's L1 from being stale.
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_pdl(void (*k)(KArgs...), int grid, int block, size_t smem, cudaStream_t st,
                               Args&&... args) {
