@@ -413,8 +413,11 @@ __global__ void __launch_bounds__(GTH, 1) k_chunk_gemm(const __grid_constant__ G
         sl1.next(nt);
         sr1.next(NSG);
         // a_ready implies full[s] (the dequantisation waited for it)
-        bool ok = wait(&bar->a_ready[sl.t], sl.ph);
-        if (n2 == 2) ok = ok && wait(&bar->a_ready[sl1.t], sl1.ph);
+        // both probes issued back to back (their latencies overlap); the bounded waits only if one is not ready
+        const bool r0 = mbar_try_wait(&bar->a_ready[sl.t], sl.ph);
+        const bool r1 = n2 == 2 ? mbar_try_wait(&bar->a_ready[sl1.t], sl1.ph) : true;
+        bool ok = r0 && r1;
+        if (!ok) ok = (r0 || wait(&bar->a_ready[sl.t], sl.ph)) && (r1 || wait(&bar->a_ready[sl1.t], sl1.ph));
         const bool last = kt + n2 == jb.ktiles;
         if (last) ok = ok && wait(&bar->bb_full[pb], (njob >> 1) & 1u);
         if (!__all_sync(0xFFFFFFFFu, ok)) { run = false; break; }
